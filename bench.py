@@ -1,0 +1,368 @@
+"""Benchmark of the decode-row trellis projection on one GB300 per process.
+
+Workload: the LM head, 5120 -> 129,280 at 4 bits per weight, one call each at
+1, 8 and 16 rows per step (fp32 logits), on seeded synthetic inputs shaped
+like the page's ("hip exl3: the input rotation and trellis linear for decode
+rows", section "What this changes": x ~ N(0,1) fp16, suh/svh random sign *
+U[0.5,1.5], uniformly random packed trellis bits).
+
+A step is the whole hot path for each row count: tf_rot_in then
+tf_trellis_linear. The packed weights (331 MB each) exceed the 129 MB L2; two
+copies alternate between calls, so no call finds its weights in L2.
+
+Metric: weight GB/s = packed weight bytes streamed / time, with the fraction
+of the measured HBM copy bandwidth it reaches. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: the path has no exchange step; N processes run N independent
+replicas (weak scaling) and rank 0 reports the aggregate.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+IN_F, OUT_F, BITS = 5120, 129280, 4
+ROWS = (1, 8, 16)
+WORKLOAD = "LM head 5120->129280, 4 bits/weight, rows {1,8,16} per step, fp32 logits"
+METRIC = "weight GB/s and % of HBM peak, trellis linear 5120->129280 @4b, 1-16 rows"
+KERNEL_SOURCES = ("linear_simple.cu", "decode.cuh", "epilogue.cuh", "ptx.cuh")
+
+
+def weight_bytes():
+    return IN_F * OUT_F * BITS // 8
+
+
+def launch_bytes(rows):
+    """Algorithmic bytes of one linear launch: packed weights, fp16 xr, fp16
+    svh, fp32 y."""
+    return weight_bytes() + rows * IN_F * 2 + OUT_F * 2 + rows * OUT_F * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "trellis_quantized_linear_rot_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "trellis_linear_head_4b.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        d = json.load(fh)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(n_blocks, rows_list, seed_base=0):
+    """The oracle on a bounded sample of the workload: n_blocks output blocks
+    of 128 (their 5120 x 128 weight slices decoded from the packed stream),
+    for each row count. Returns (seconds, weight bytes covered)."""
+    import numpy as np
+    from oracle import exl3 as o
+    from trellis_quantized_linear_rot_gb300 import synth
+    kt, nt = IN_F // 16, OUT_F // 16
+    g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS + seed_base))
+    # Only the sampled blocks' tiles are drawn (same distribution as the full stream).
+    tr = g.integers(0, 2**32, size=kt * 8 * n_blocks * 8 * BITS, dtype=np.uint32)
+    x = synth.make_x(max(rows_list), IN_F, synth.SEED_X + 2)
+    suh = synth.make_scale(IN_F, synth.SEED_SUH + 2)
+    svh = synth.make_scale(128 * n_blocks, synth.SEED_SVH + 2)
+    i_small = IN_F
+    t0 = time.perf_counter()
+    covered = 0
+    for rows in rows_list:
+        xr = o.rot_in_f32(x[:rows], suh)
+        w = o.decode_matrix(tr, i_small, 128 * n_blocks, BITS)
+        o.linear_f64(xr, w, svh)
+        covered += i_small * 128 * n_blocks * BITS // 8
+    return time.perf_counter() - t0, covered
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle timed on the host cores: each step is a bounded sample of
+    the workload (2 output blocks, each row count)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    n_blocks = 2
+    for _ in range(args.warmup):
+        oracle_sample(n_blocks, ROWS)
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        t, b = oracle_sample(n_blocks, ROWS)
+        total_t += t
+        total_b += b
+    value = total_b / total_t / 1e9
+    sample = "%d of 1010 output blocks (5120x128 weights each) per row count, rows {1,8,16}" % n_blocks
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F,
+                                        "out_features": OUT_F, "bits": BITS},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "host_threads_available": cpu_threads()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import trellis_quantized_linear_rot_gb300 as tf
+    from trellis_quantized_linear_rot_gb300 import synth
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # Inputs (untimed): two copies of the packed weights, x for 16 rows.
+    tr_np = synth.make_trellis(IN_F, OUT_F, BITS, synth.SEED_TRELLIS + 2 + BITS)
+    tr0 = torch.from_numpy(tr_np.view(np.int32)).to(dev)
+    tr1 = tr0.clone()
+    del tr_np
+    trs = (tr0, tr1)
+    x = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).to(dev)
+    suh = torch.from_numpy(synth.make_scale(IN_F, synth.SEED_SUH + 2)).to(dev)
+    svh = torch.from_numpy(synth.make_scale(OUT_F, synth.SEED_SVH + 2)).to(dev)
+    xrs = {r: torch.empty((r, IN_F), dtype=torch.float16, device=dev) for r in ROWS}
+    ys = {r: torch.empty((r, OUT_F), dtype=torch.float32, device=dev) for r in ROWS}
+    ev = {r: [] for r in ROWS}
+    call = [0]
+
+    def step(record):
+        for r in ROWS:
+            tf.tf_rot_in(x[:r], suh, xr=xrs[r])
+            t = trs[call[0] % 2]
+            call[0] += 1
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            tf.tf_trellis_linear(xrs[r], t, svh, BITS, OUT_F, y=ys[r])
+            if record:
+                e1.record(stream)
+                ev[r].append((e0, e1))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    tf.tf_device_error()
+    barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    tf.tf_device_error()
+    ms_total = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    bytes_step = weight_bytes() * len(ROWS)
+    value = bytes_step * args.steps * world / (ms_total * 1e-3) / 1e9
+
+    # Dominant kernel: the linear launches, timed by events on their stream.
+    per_rows = {}
+    dur_sum, byte_sum = 0.0, 0
+    for r in ROWS:
+        ds = [a.elapsed_time(b) for a, b in ev[r]]
+        per_rows[r] = {"us_median": statistics.median(ds) * 1e3,
+                       "weight_gbs": weight_bytes() / (statistics.median(ds) * 1e-3) / 1e9}
+        dur_sum += sum(ds)
+        byte_sum += launch_bytes(r) * len(ds)
+    achieved = byte_sum / (dur_sum * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic()
+
+    # End to end through the public API from pinned host memory.
+    x_host = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).pin_memory()
+    y_host = {r: torch.empty((r, OUT_F), dtype=torch.float32).pin_memory() for r in ROWS}
+    e2e_steps = max(2, min(args.steps, 10))
+
+    def e2e_step():
+        for r in ROWS:
+            xd = x_host[:r].to(dev, non_blocking=True)
+            y = tf.project(xd, suh, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
+            call[0] += 1
+            y_host[r].copy_(y, non_blocking=True)
+        torch.cuda.synchronize()
+
+    e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = bytes_step * e2e_steps * world / e2e_s / 1e9
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        n_blocks = 16
+        secs, covered = oracle_sample(n_blocks, ROWS)
+        cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of 1010 output blocks (5120x128 weights each) for each of rows {1,8,16}, "
+                         "%.1f s" % (n_blocks, secs),
+               "host_threads_available": cpu_threads()}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 (fp32 sums)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F, "out_features": OUT_F,
+                   "bits": BITS, "out_dtype": "fp32", "weight_bytes_per_call": weight_bytes(),
+                   "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "by_rows": per_rows,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": "trellis_linear", "kernel_hash": kernel_hash()},
+        "clocks": clocks.summary(),
+        "e2e": {"value": e2e_value, "unit": "GB/s",
+                "h2d_bytes_per_step": sum(r * IN_F * 2 for r in ROWS),
+                "d2h_bytes_per_step": sum(r * OUT_F * 4 for r in ROWS)},
+        "gpu_launches": 2 * len(ROWS) * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

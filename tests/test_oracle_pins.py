@@ -461,3 +461,12 @@ def test_planted_transposed_tile_is_caught():
     wt = np.swapaxes(o.decode_tiles(t, k), -1, -2)    # n, k swapped inside tiles
     bad = wt.transpose(0, 2, 1, 3).reshape(128, 128)
     assert not np.array_equal(bits16(bad), bits16(w))
+
+
+def test_decode_rows_and_blocks_agree_with_matrix():
+    k = 5
+    tr = synth.make_trellis(256, 256, k, 81)
+    w = o.decode_matrix(tr, 256, 256, k)
+    ks = [0, 17, 255]
+    assert np.array_equal(bits16(o.decode_rows(tr, 256, 256, k, ks)), bits16(w[ks]))
+    assert np.array_equal(bits16(o.decode_blocks(tr, 256, 256, k, [1])), bits16(w[:, 128:]))

@@ -1,0 +1,44 @@
+// Internal launchers shared by the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace tfx {
+
+cudaError_t launch_rot_in(const void* x, int x_dtype, const __half* suh, __half* xr, int rows,
+                          int in_features, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_trellis_decode(const uint32_t* trellis, __half* w, int in_features,
+                                  int out_features, int bits, cudaStream_t stream);
+
+// One pass of at most 16 rows through the trellis linear.
+struct LinearPass {
+  const __half* xr;          // [rows][in] fp16
+  const uint32_t* trellis;   // packed tiles
+  const __half* svh;         // [out]
+  void* y;                   // [rows][out]
+  int out_f32;               // 1: fp32 output, 0: fp16
+  int rows;                  // 1..16
+  int in_features;
+  int out_features;
+  int bits;
+};
+
+// Per-device state the linear needs: SM count, error flag, partial-sum
+// workspace for output blocks shared by several CTAs.
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  int* err_flag = nullptr;       // device int, OR of error bits
+  float* partials = nullptr;     // [slots][16][128] fp32
+  int* counters = nullptr;       // [max_blocks] arrival counters, kept at zero between calls
+  size_t partial_slots = 0;
+  size_t counter_len = 0;
+};
+
+cudaError_t launch_trellis_linear_simple(const LinearPass& p, int* err_flag, cudaStream_t stream);
+
+}  // namespace tfx
