@@ -36,7 +36,7 @@ IN_F, OUT_F, BITS = 5120, 129280, 4
 ROWS = (1, 8, 16)
 WORKLOAD = "LM head 5120->129280, 4 bits/weight, rows {1,8,16} per step, fp32 logits"
 METRIC = "weight GB/s and % of HBM peak, trellis linear 5120->129280 @4b, 1-16 rows"
-KERNEL_SOURCES = ("linear_simple.cu", "decode.cuh", "epilogue.cuh", "ptx.cuh")
+KERNEL_SOURCES = ("linear_tc.cu", "decode.cuh", "epilogue.cuh", "ptx.cuh")
 
 
 def weight_bytes():
@@ -95,7 +95,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -141,28 +141,28 @@ def dist_env():
     return world, rank, local
 
 
-def oracle_sample(n_blocks, rows_list, seed_base=0):
-    """The oracle on a bounded sample of the workload: n_blocks output blocks
-    of 128 (their 5120 x 128 weight slices decoded from the packed stream),
-    for each row count. Returns (seconds, weight bytes covered)."""
+def oracle_sample(n_blocks, rows_list, k_tiles=IN_F // 16):
+    """The oracle on a bounded sample of the workload: the weights of n_blocks
+    output blocks of 128 over the first k_tiles * 16 inputs (decoded from a
+    packed stream of the same distribution), for each row count: rot_in,
+    decode, float64 linear and output rotation. Returns (seconds, packed
+    weight bytes covered)."""
     import numpy as np
     from oracle import exl3 as o
     from trellis_quantized_linear_rot_gb300 import synth
-    kt, nt = IN_F // 16, OUT_F // 16
-    g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS + seed_base))
-    # Only the sampled blocks' tiles are drawn (same distribution as the full stream).
-    tr = g.integers(0, 2**32, size=kt * 8 * n_blocks * 8 * BITS, dtype=np.uint32)
-    x = synth.make_x(max(rows_list), IN_F, synth.SEED_X + 2)
-    suh = synth.make_scale(IN_F, synth.SEED_SUH + 2)
+    i_s = 128 * max(1, k_tiles // 8)
+    g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS))
+    tr = g.integers(0, 2**32, size=i_s * 128 * n_blocks * BITS // 32, dtype=np.uint32)
+    x = synth.make_x(max(rows_list), i_s, synth.SEED_X + 2)
+    suh = synth.make_scale(i_s, synth.SEED_SUH + 2)
     svh = synth.make_scale(128 * n_blocks, synth.SEED_SVH + 2)
-    i_small = IN_F
     t0 = time.perf_counter()
     covered = 0
     for rows in rows_list:
         xr = o.rot_in_f32(x[:rows], suh)
-        w = o.decode_matrix(tr, i_small, 128 * n_blocks, BITS)
+        w = o.decode_matrix(tr, i_s, 128 * n_blocks, BITS)
         o.linear_f64(xr, w, svh)
-        covered += i_small * 128 * n_blocks * BITS // 8
+        covered += i_s * 128 * n_blocks * BITS // 8
     return time.perf_counter() - t0, covered
 
 
@@ -174,21 +174,26 @@ def cpu_threads():
 
 
 def run_reference(args):
-    """The oracle timed on the host cores: each step is a bounded sample of
-    the workload (2 output blocks, each row count)."""
+    """The oracle timed on the host cores, on the same workload and metric.
+    Each step is a bounded sample of it (one output block over a slice of the
+    inputs, for each row count), sized so that the whole run of warm-up and
+    timed steps takes about two minutes."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    n_blocks = 2
+    t_cal, _ = oracle_sample(1, ROWS, k_tiles=8)          # 128 inputs x 128 outputs
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    k_tiles = int(max(8, min(IN_F // 16, 8 * per_step / max(t_cal, 1e-6))))
     for _ in range(args.warmup):
-        oracle_sample(n_blocks, ROWS)
+        oracle_sample(1, ROWS, k_tiles)
     total_t, total_b = 0.0, 0
     for _ in range(args.steps):
-        t, b = oracle_sample(n_blocks, ROWS)
+        t, b = oracle_sample(1, ROWS, k_tiles)
         total_t += t
         total_b += b
     value = total_b / total_t / 1e9
-    sample = "%d of 1010 output blocks (5120x128 weights each) per row count, rows {1,8,16}" % n_blocks
+    sample = ("1 of 1010 output blocks over %d of 5120 inputs per row count (rows {1,8,16}) per step"
+              % (128 * max(1, k_tiles // 8)))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
@@ -299,17 +304,19 @@ def run_ours(args):
             y_host[r].copy_(y, non_blocking=True)
         torch.cuda.synchronize()
 
-    e2e_step()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    e2e_s = float("nan")
+    if not args.no_e2e:
         e2e_step()
-    e2e_s = time.perf_counter() - t0
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e2e_s = time.perf_counter() - t0
     if dist is not None:
         t = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
-    e2e_value = bytes_step * e2e_steps * world / e2e_s / 1e9
+    e2e_value = bytes_step * e2e_steps * world / e2e_s / 1e9 if not args.no_e2e else None
 
     if rank != 0:
         if dist is not None:
@@ -318,7 +325,7 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_blocks = 16
+        n_blocks = 48
         secs, covered = oracle_sample(n_blocks, ROWS)
         cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "%d of 1010 output blocks (5120x128 weights each) for each of rows {1,8,16}, "
@@ -337,9 +344,10 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                      "kernel": "trellis_linear", "kernel_hash": kernel_hash()},
         "clocks": clocks.summary(),
-        "e2e": {"value": e2e_value, "unit": "GB/s",
-                "h2d_bytes_per_step": sum(r * IN_F * 2 for r in ROWS),
-                "d2h_bytes_per_step": sum(r * OUT_F * 4 for r in ROWS)},
+        "e2e": None if args.no_e2e else {
+            "value": e2e_value, "unit": "GB/s",
+            "h2d_bytes_per_step": sum(r * IN_F * 2 for r in ROWS),
+            "d2h_bytes_per_step": sum(r * OUT_F * 4 for r in ROWS)},
         "gpu_launches": 2 * len(ROWS) * args.steps,
         "cpu_baseline": cpu,
     }
@@ -351,13 +359,17 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    global ROWS
+    ROWS = tuple(int(r) for r in args.rows.split(","))
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -65,6 +65,37 @@ tf_status current_ctx(DeviceCtx** out) {
   return TF_OK;
 }
 
+// The linear's workspace on the current device: partial sums for up to one
+// CTA per SM and one arrival counter per possible output block, allocated
+// and zeroed once, on the first call that needs it.
+tf_status ensure_workspace(DeviceCtx* c) {
+  std::lock_guard<std::mutex> lock(g_ctx_mutex);
+  if (c->partials != nullptr) return TF_OK;
+  const size_t slots = static_cast<size_t>(c->num_sms) * 2;
+  const size_t counters = kMaxOutFeatures / 128;
+  void* part = nullptr;
+  void* cnt = nullptr;
+  cudaError_t e = cudaMalloc(&part, slots * 16 * 128 * sizeof(float));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (workspace)");
+  e = cudaMalloc(&cnt, counters * sizeof(int));
+  if (e != cudaSuccess) {
+    cudaFree(part);
+    return cuda_fail(e, "cudaMalloc (workspace)");
+  }
+  e = cudaMemset(cnt, 0, counters * sizeof(int));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(part);
+    cudaFree(cnt);
+    return cuda_fail(e, "cudaMemset (workspace)");
+  }
+  c->partials = static_cast<float*>(part);
+  c->counters = static_cast<int*>(cnt);
+  c->partial_slots = slots;
+  c->counter_len = counters;
+  return TF_OK;
+}
+
 // The pointer must be device (or managed) memory of `device`.
 tf_status check_device_ptr(const void* p, int device) {
   cudaPointerAttributes attr;
@@ -157,6 +188,13 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
   if (s != TF_OK) return s;
   s = check_device_ptrs(ctx->device, xr, trellis, svh, y);
   if (s != TF_OK) return s;
+  s = ensure_workspace(ctx);
+  if (s != TF_OK) return s;
+  TcWorkspace ws;
+  ws.partials = ctx->partials;
+  ws.counters = ctx->counters;
+  ws.err_flag = ctx->err_flag;
+  ws.ctas = trellis_linear_tc_ctas(ctx->num_sms, in_features, out_features);
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
   for (int r0 = 0; r0 < rows; r0 += 16) {
     LinearPass p;
@@ -169,7 +207,7 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
     p.in_features = in_features;
     p.out_features = out_features;
     p.bits = bits;
-    cudaError_t e = launch_trellis_linear_simple(p, ctx->err_flag, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_trellis_linear_tc(p, ws, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "trellis linear launch");
   }
   return TF_OK;
@@ -206,7 +244,10 @@ tf_status tf_device_error(void* stream) {
   if (flag != 0) {
     const int zero = 0;
     e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    if (e == cudaSuccess && ctx->counters != nullptr)
+      e = cudaMemset(ctx->counters, 0, ctx->counter_len * sizeof(int));  // an aborted launch may leave counts
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "resetting the error record");
     return TF_ERR_TIMEOUT;
   }
   return TF_OK;

@@ -57,22 +57,14 @@ __device__ __forceinline__ int row_first_bit(int n) {
   return (16 * n * BITS + BITS - 16 + RowSpan<BITS>::kTileBits) % RowSpan<BITS>::kTileBits;
 }
 
-// Decodes output column n (0..15) of the tile whose words start at `tw`.
-// `Load` reads word w (0 <= w < 8*bits) of the tile.
-template <int BITS, typename Load>
-__device__ __forceinline__ void decode_col16(Load load, int n, uint32_t (&out)[8]) {
+// Generic width: the thread's words w[0..kWords) start at word
+// row_first_bit(n) / 32 (circularly); they are first aligned so that the
+// first window starts at the top bit, then window j is cut out at bit j*bits.
+template <int BITS>
+__device__ __forceinline__ void decode_words_generic(const uint32_t (&wv)[RowSpan<BITS>::kWords], int n,
+                                                     uint32_t (&out)[8]) {
   using S = RowSpan<BITS>;
-  const int p0 = row_first_bit<BITS>(n);
-  const int w0 = p0 >> 5;
-  const int off = p0 & 31;
-  uint32_t wv[S::kWords];
-#pragma unroll
-  for (int j = 0; j < S::kWords; ++j) {
-    int wi = w0 + j;
-    wi = (wi >= S::kTileWords) ? wi - S::kTileWords : wi;
-    wv[j] = load(wi);
-  }
-  // Align so that stream bit p0 is the most significant bit of a[0].
+  const int off = row_first_bit<BITS>(n) & 31;
   uint32_t a[S::kWords - 1];
 #pragma unroll
   for (int j = 0; j < S::kWords - 1; ++j) a[j] = __funnelshift_l(wv[j + 1], wv[j], off);
@@ -86,6 +78,78 @@ __device__ __forceinline__ void decode_col16(Load load, int n, uint32_t (&out)[8
   }
 #pragma unroll
   for (int c = 0; c < 8; ++c) out[c] = mul1_pair(h[2 * c], h[2 * c + 1]);
+}
+
+// 4 bits: a tile is 32 words; output column n's windows start at stream bit
+// 64n - 12, i.e. at bit 20 of word a = (2n - 1) mod 32, and run through words
+// b = 2n and c = 2n + 1; window j covers bits [20 + 4j, 36 + 4j) of a:b:c.
+// Each window is cut out with one byte permute, shift or mask from a word
+// or a funnel-shifted pair, six helper shifts serving all sixteen.
+__device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xFFFFu; }
+__device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
+__device__ __forceinline__ uint32_t mid16(uint32_t x) { return __byte_perm(x, 0u, 0x4421); }
+
+__device__ __forceinline__ void decode_col16_b4(uint32_t a, uint32_t b, uint32_t c, uint32_t (&out)[8]) {
+  const uint32_t p = __funnelshift_l(b, a, 12);   // stream bits 12..43 (of a:b:c)
+  const uint32_t m = __funnelshift_l(b, a, 16);   // 16..47
+  const uint32_t b4 = b >> 4;                     // 28..59, top nibble zero
+  const uint32_t p2 = __funnelshift_l(c, b, 12);  // 44..75
+  const uint32_t m2 = __funnelshift_l(c, b, 16);  // 48..79
+  const uint32_t c4 = c >> 4;                     // 60..91
+  const uint32_t st[16] = {mid16(p),  mid16(m),  lo16(p),  hi16(b), mid16(b4), mid16(b),
+                           lo16(b4),  lo16(b),   mid16(p2), mid16(m2), lo16(p2), hi16(c),
+                           mid16(c4), mid16(c),  lo16(c4), lo16(c)};
+  uint32_t h[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) h[j] = mul1_half_plus_1024(st[j]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
+}
+
+// Two-step form used by the pipelined linear: first every word a column
+// needs (loads only), then the arithmetic, so a thread can issue the loads of
+// several k-tiles before it needs any of them.
+template <int BITS>
+struct ColWords {
+  static constexpr int kCount = BITS == 4 ? 3 : RowSpan<BITS>::kWords;
+  uint32_t w[kCount];
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWords<BITS>& cw) {
+  if constexpr (BITS == 4) {
+    cw.w[0] = tw[(2 * n + 31) & 31];
+    const uint2 bc = *reinterpret_cast<const uint2*>(tw + 2 * n);
+    cw.w[1] = bc.x;
+    cw.w[2] = bc.y;
+  } else {
+    using S = RowSpan<BITS>;
+    const int w0 = row_first_bit<BITS>(n) >> 5;
+#pragma unroll
+    for (int j = 0; j < S::kWords; ++j) {
+      int wi = w0 + j;
+      wi = (wi >= S::kTileWords) ? wi - S::kTileWords : wi;
+      cw.w[j] = tw[wi];
+    }
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ void decode_col_words(const ColWords<BITS>& cw, int n, uint32_t (&out)[8]) {
+  if constexpr (BITS == 4) {
+    decode_col16_b4(cw.w[0], cw.w[1], cw.w[2], out);
+  } else {
+    decode_words_generic<BITS>(cw.w, n, out);
+  }
+}
+
+// Decodes column n of the tile at `tw` (a pointer into shared or global
+// memory), using the fast path where one exists.
+template <int BITS>
+__device__ __forceinline__ void decode_col16_ptr(const uint32_t* tw, int n, uint32_t (&out)[8]) {
+  ColWords<BITS> cw;
+  load_col_words<BITS>(tw, n, cw);
+  decode_col_words<BITS>(cw, n, out);
 }
 
 }  // namespace tfx

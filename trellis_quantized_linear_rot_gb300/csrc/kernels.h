@@ -39,6 +39,17 @@ struct DeviceCtx {
   size_t counter_len = 0;
 };
 
-cudaError_t launch_trellis_linear_simple(const LinearPass& p, int* err_flag, cudaStream_t stream);
+// Workspace of the persistent linear: partial sums of output blocks cut
+// between CTAs ([ctas][2][16][128] fp32) and one arrival counter per output
+// block (zero between calls).
+struct TcWorkspace {
+  float* partials;
+  int* counters;
+  int* err_flag;
+  int ctas;
+};
+
+int trellis_linear_tc_ctas(int num_sms, int in_features, int out_features);
+cudaError_t launch_trellis_linear_tc(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream);
 
 }  // namespace tfx
