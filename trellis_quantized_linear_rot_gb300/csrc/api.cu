@@ -194,7 +194,7 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
   ws.partials = ctx->partials;
   ws.counters = ctx->counters;
   ws.err_flag = ctx->err_flag;
-  ws.ctas = trellis_linear_tc_ctas(ctx->num_sms, in_features, out_features);
+  ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features);
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
   for (int r0 = 0; r0 < rows; r0 += 16) {
     LinearPass p;
@@ -207,7 +207,7 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
     p.in_features = in_features;
     p.out_features = out_features;
     p.bits = bits;
-    cudaError_t e = launch_trellis_linear_tc(p, ws, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_trellis_linear_mma(p, ws, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "trellis linear launch");
   }
   return TF_OK;

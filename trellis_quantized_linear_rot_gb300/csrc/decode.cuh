@@ -106,12 +106,32 @@ __device__ __forceinline__ void decode_col16_b4(uint32_t a, uint32_t b, uint32_t
   for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
 }
 
+// 8 bits: a tile is 64 words; output column n's windows start at stream bit
+// 128n - 8, i.e. at bit 24 of word a = (4n - 1) mod 64, and run through words
+// b..e = 4n .. 4n+3; window j covers bits [24 + 8j, 40 + 8j) of a:b:c:d:e, so
+// every window is byte aligned: one byte permute, shift or mask each, plus a
+// funnel shift for each of the four windows that straddle two words.
+__device__ __forceinline__ void decode_col16_b8(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t e, uint32_t (&out)[8]) {
+  const uint32_t ab = __funnelshift_l(b, a, 16);
+  const uint32_t bc = __funnelshift_l(c, b, 16);
+  const uint32_t cd = __funnelshift_l(d, c, 16);
+  const uint32_t de = __funnelshift_l(e, d, 16);
+  const uint32_t st[16] = {mid16(ab), hi16(b), mid16(b), lo16(b), mid16(bc), hi16(c), mid16(c), lo16(c),
+                           mid16(cd), hi16(d), mid16(d), lo16(d), mid16(de), hi16(e), mid16(e), lo16(e)};
+  uint32_t h[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) h[j] = mul1_half_plus_1024(st[j]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
+}
+
 // Two-step form used by the pipelined linear: first every word a column
 // needs (loads only), then the arithmetic, so a thread can issue the loads of
 // several k-tiles before it needs any of them.
 template <int BITS>
 struct ColWords {
-  static constexpr int kCount = BITS == 4 ? 3 : RowSpan<BITS>::kWords;
+  static constexpr int kCount = BITS == 4 ? 3 : (BITS == 8 ? 5 : RowSpan<BITS>::kWords);
   uint32_t w[kCount];
 };
 
@@ -122,6 +142,13 @@ __device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWor
     const uint2 bc = *reinterpret_cast<const uint2*>(tw + 2 * n);
     cw.w[1] = bc.x;
     cw.w[2] = bc.y;
+  } else if constexpr (BITS == 8) {
+    cw.w[0] = tw[(4 * n + 63) & 63];
+    const uint4 be = *reinterpret_cast<const uint4*>(tw + 4 * n);
+    cw.w[1] = be.x;
+    cw.w[2] = be.y;
+    cw.w[3] = be.z;
+    cw.w[4] = be.w;
   } else {
     using S = RowSpan<BITS>;
     const int w0 = row_first_bit<BITS>(n) >> 5;
@@ -138,6 +165,8 @@ template <int BITS>
 __device__ __forceinline__ void decode_col_words(const ColWords<BITS>& cw, int n, uint32_t (&out)[8]) {
   if constexpr (BITS == 4) {
     decode_col16_b4(cw.w[0], cw.w[1], cw.w[2], out);
+  } else if constexpr (BITS == 8) {
+    decode_col16_b8(cw.w[0], cw.w[1], cw.w[2], cw.w[3], cw.w[4], out);
   } else {
     decode_words_generic<BITS>(cw.w, n, out);
   }
@@ -150,6 +179,56 @@ __device__ __forceinline__ void decode_col16_ptr(const uint32_t* tw, int n, uint
   ColWords<BITS> cw;
   load_col_words<BITS>(tw, n, cw);
   decode_col_words<BITS>(cw, n, out);
+}
+
+// ---------------------------------------------------------------------------
+// Fragment form for mma.sync.m16n8k16 with A = W^T (16 outputs x 16 inputs).
+// Lane (g, t) = (lane / 4, lane % 4) owns outputs g and g + 8 of the tile at
+// inputs 4t .. 4t+3 (the MMA's k positions 2t, 2t+1, 2t+8, 2t+9 are mapped to
+// those four inputs; the B operand uses the same map). A group of four
+// consecutive stream weights of output n starts at stream bit
+// (16n + 4t) * bits + bits - 16 and spans 3 * bits + 16 bits.
+template <int BITS>
+struct Group4 {
+  static constexpr int kTileWords = 8 * BITS;
+  static constexpr int kTileBits = 256 * BITS;
+  static constexpr int kWords = (3 * BITS + 16 + 31 <= 64) ? 2 : 3;
+};
+
+// Packs weights (4t, 4t+1) and (4t+2, 4t+3) of output n as two half2 words.
+template <int BITS>
+__device__ __forceinline__ void decode_group4(const uint32_t* tw, int n, int t, uint32_t& lo, uint32_t& hi) {
+  using G = Group4<BITS>;
+  const int start = ((16 * n + 4 * t) * BITS + BITS - 16 + G::kTileBits) % G::kTileBits;
+  const int w0 = start >> 5;
+  const int off = start & 31;
+  uint32_t s[4];
+  if constexpr (G::kWords == 2) {
+    const int w1 = (w0 + 1 == G::kTileWords) ? 0 : w0 + 1;
+    const uint32_t x0 = tw[w0];
+    const uint32_t x1 = tw[w1];
+    const uint32_t p = __funnelshift_l(x1, x0, off);  // the group's bits, first window at the top
+    if constexpr (BITS == 4) {
+      const uint32_t p4 = p >> 4;
+      s[0] = hi16(p);
+      s[1] = mid16(p4);
+      s[2] = mid16(p);
+      s[3] = lo16(p4);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[j] = (p >> (16 - j * BITS)) & 0xFFFFu;
+    }
+  } else {
+    const int w1 = (w0 + 1 == G::kTileWords) ? 0 : w0 + 1;
+    const int w2 = (w1 + 1 == G::kTileWords) ? 0 : w1 + 1;
+    const uint32_t x0 = tw[w0], x1 = tw[w1], x2 = tw[w2];
+    const uint32_t a0 = __funnelshift_l(x1, x0, off);
+    const uint32_t a1 = __funnelshift_l(x2, x1, off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = __funnelshift_l(a1, a0, j * BITS) >> 16;
+  }
+  lo = mul1_pair(mul1_half_plus_1024(s[0]), mul1_half_plus_1024(s[1]));
+  hi = mul1_pair(mul1_half_plus_1024(s[2]), mul1_half_plus_1024(s[3]));
 }
 
 }  // namespace tfx

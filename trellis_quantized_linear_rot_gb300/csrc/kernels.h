@@ -49,7 +49,7 @@ struct TcWorkspace {
   int ctas;
 };
 
-int trellis_linear_tc_ctas(int num_sms, int in_features, int out_features);
-cudaError_t launch_trellis_linear_tc(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream);
+int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features);
+cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream);
 
 }  // namespace tfx

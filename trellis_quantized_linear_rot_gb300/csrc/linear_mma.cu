@@ -1,0 +1,423 @@
+// The trellis linear for decode rows on GB300: a persistent kernel with a
+// TMA-fed shared-memory pipeline; the weights are decoded straight into
+// tensor-core operand registers and multiplied with mma.sync.m16n8k16.
+//
+// Method: "hip exl3: the input rotation and trellis linear for decode rows",
+// section "What this changes" (second bullet): the trellis linear at 2..8 bits
+// with mul1, one fp16 fma per decoded weight, each row's K sums in a fixed
+// order (so a row's bits do not depend on the rows sharing its launch), no
+// bias; the output rotation and svh finish each 128-output block.
+//
+// Why mma.sync and not tcgen05: the contraction per 16 x 16 weight tile has at
+// most 16 columns (the rows of a pass). tcgen05.mma (M = 128, N = 16) measured
+// 45-56 cycles per instruction from its single issuing thread, about 110 when
+// that thread shares its SM sub-partition with decode warps, and needs the
+// decoded weights staged through Tensor Memory; mma.sync.m16n8k16 measured 2.2
+// cycles per instruction per SM, takes the A operand straight from the decode
+// registers and is issued by every compute warp, so the contraction spreads
+// over all four sub-partitions and never stalls the decode.
+//
+// Work: the (output block b, 128-input unit) grid, block-major, is cut into
+// one contiguous range per CTA (one CTA per SM). Consecutive units of one block
+// form a segment; a segment's sums accumulate in registers in input order. A
+// block whose units all belong to one CTA is finished by it; a block cut
+// between CTAs has each CTA publish its partial sums, and the CTA that arrives
+// last adds them in CTA order (the input order) and finishes the block. The
+// cut depends only on the shape and the CTA count, never on the rows.
+//
+// Warp roles:
+//   warps 0-3   epilogue: sums of a finished segment (from shared memory) ->
+//               output rotation -> svh -> y, or the cross-CTA partial sums
+//   warps 4-11  compute: warp 4 + j owns output tile j (outputs 16j..16j+15 of
+//               the block); per unit it decodes its 8 tiles (one per k-tile)
+//               into A fragments and issues one mma.sync per 8 rows per tile
+//   warp 12     producer: one thread issues the TMA copies of each unit
+//               (packed weights of 8 k-tiles x 8 tiles; the 16 x 128 slice of
+//               xr, 128-byte swizzled so the B-fragment loads hit distinct
+//               banks)
+// All waits are bounded; a kernel that gives up sets the error flag and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "decode.cuh"
+#include "epilogue.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace tfx {
+
+namespace {
+
+constexpr int kUnitKt = 8;           // k-tiles per unit (128 inputs)
+constexpr int kXrUnitBytes = 4096;   // 16 rows x 128 inputs fp16 (two 64-input halves)
+constexpr int kComputeWarps = 8;     // one per 16-output tile of a block
+constexpr int kThreads = (4 + kComputeWarps + 1) * 32;
+constexpr int kSmemBudget = 196 * 1024;
+
+template <int BITS>
+struct Cfg {
+  static constexpr int kWUnitBytes = 2048 * BITS;  // 8 k-tiles x 8 tiles x 32*BITS bytes
+  static constexpr int kStageBytes = kWUnitBytes + kXrUnitBytes;
+  static constexpr int kStagesFit = (kSmemBudget - 3 * 8192 - 1024) / kStageBytes;
+  static constexpr int kStages = kStagesFit < 12 ? kStagesFit : 12;
+};
+
+struct MmaParams {
+  const __half* svh;
+  void* y;
+  float* partials;      // [ctas][2][16][128]
+  int* counters;        // [out_features / 128]
+  int* err_flag;
+  long long units;      // (out/128) * (in/128)
+  int units_per_block;  // in / 128
+  int ctas;
+  int out_f32;
+  int rows;
+  int in_features;
+  int out_features;
+};
+
+__device__ __forceinline__ long long range_start(long long c, long long units, int ctas) {
+  return c * units / ctas;
+}
+
+// CTA whose range holds unit u.
+__device__ __forceinline__ int cta_of_unit(long long u, long long units, int ctas) {
+  return static_cast<int>(((u + 1) * ctas - 1) / units);
+}
+
+// Slot of a CTA's partial sums for block b: 0 for the first block of its
+// range, 1 for the last (a CTA's range cuts at most two blocks).
+__device__ __forceinline__ int partial_slot(int c, int b, const MmaParams& p) {
+  const long long first_block = range_start(c, p.units, p.ctas) / p.units_per_block;
+  return b == first_block ? 0 : 1;
+}
+
+template <int BITS>
+struct Layout {
+  static constexpr int kStages = Cfg<BITS>::kStages;
+  static constexpr int kStageBytes = Cfg<BITS>::kStageBytes;
+  static constexpr int kDbufOff = kStages * kStageBytes;        // 2 x [16][128] fp32 segment sums
+  static constexpr int kXchOff = kDbufOff + 2 * 8192;            // [16][128] fp32 for the rotation
+  static constexpr int kBarOff = kXchOff + 8192;
+  static constexpr int kNumBars = 2 * kStages + 4;               // full, empty, dfull[2], dempty[2]
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kUsed = kMiscOff + 64;
+  // At least 120 KB, so that two CTAs never share an SM.
+  static constexpr int kBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int BITS, bool TWO_HALVES>
+__global__ void __launch_bounds__(kThreads, 1)
+    trellis_linear_mma_kernel(const __grid_constant__ CUtensorMap wmap,
+                              const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
+  using L = Layout<BITS>;
+  constexpr int S = L::kStages;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  float* dbuf = reinterpret_cast<float*>(smem + L::kDbufOff);
+  float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + L::kXchOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * S + d); };
+  auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 + d); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kProducerWarp = 4 + kComputeWarps;
+  const int c = blockIdx.x;
+  const long long u0 = range_start(c, p.units, p.ctas);
+  const long long u1 = range_start(c + 1, p.units, p.ctas);
+  const int n_units = static_cast<int>(u1 - u0);
+  const int UB = p.units_per_block;
+  const long long b_first = u0 / UB;
+  const long long b_last = (u1 - 1) / UB;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *last_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kComputeWarps);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(dfull_bar(d), kComputeWarps);
+      mbar_init(dempty_bar(d), 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
+  }
+  __syncthreads();
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_units; ++i) {
+        const int s = i % S;
+        const int k = i / S;
+        if (k > 0 && !mbar_wait(empty_bar(s), (k - 1) & 1, abort_flag)) break;
+        const long long u = u0 + i;
+        const int b = static_cast<int>(u / UB);
+        const int ub = static_cast<int>(u % UB);
+        const uint32_t st = smem_u32(smem + s * L::kStageBytes);
+        const uint32_t xs = st + Cfg<BITS>::kWUnitBytes;
+        mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
+        tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(s));
+        tma_load_2d(xs, &xmap, ub * 128, 0, full_bar(s));
+        tma_load_2d(xs + 2048, &xmap, ub * 128 + 64, 0, full_bar(s));
+        issued = i + 1;
+      }
+      // Let every copy this CTA started land before it can exit.
+      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
+        volatile int never = 0;
+        mbar_wait(full_bar(i % S), (i / S) & 1, &never);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------- compute
+    const int j = warp - 4;   // output tile of the block
+    const int g = lane >> 2;  // outputs g and g + 8 of the tile
+    const int t = lane & 3;   // inputs 4t .. 4t+3 of each k-tile
+    float d0[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 0..7
+    float d1[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 8..15
+    for (int i = 0; i < n_units; ++i) {
+      const long long u = u0 + i;
+      const int ub = static_cast<int>(u % UB);
+      const bool seg_last = (i == n_units - 1) || ub == UB - 1;
+      const int s = i % S;
+      const bool ok = mbar_wait(full_bar(s), (i / S) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* st = smem + s * L::kStageBytes;
+      const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
+      const uint8_t* xs = st + Cfg<BITS>::kWUnitBytes;
+#pragma unroll
+      for (int kt = 0; kt < kUnitKt; ++kt) {
+        const uint32_t* tw = wtile + kt * 64 * BITS;
+        uint32_t a[4];
+        decode_group4<BITS>(tw, g, t, a[0], a[2]);
+        decode_group4<BITS>(tw, g + 8, t, a[1], a[3]);
+        // xr row r, inputs 16kt + 4t .. +3: 128-byte swizzled rows, 16-byte
+        // chunk c of row r stored at chunk c ^ (r % 8).
+        const int chunk = 2 * (kt & 3) + (t >> 1);
+        const int off = (kt >> 2) * 2048 + ((chunk ^ g) << 4) + (t & 1) * 8;
+        const uint2 b_lo = *reinterpret_cast<const uint2*>(xs + off + g * 128);
+        mma_16816(d0, a, b_lo.x, b_lo.y);
+        if (TWO_HALVES) {
+          const uint2 b_hi = *reinterpret_cast<const uint2*>(xs + off + (g + 8) * 128);
+          mma_16816(d1, a, b_hi.x, b_hi.y);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (seg_last) {
+        const int sg = static_cast<int>((u / UB) - b_first);
+        const int d = sg & 1;
+        bool ok2 = true;
+        if (sg >= 2) ok2 = mbar_wait(dempty_bar(d), ((sg >> 1) - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok2)) break;
+        // D fragment: (output g, row 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+        float* db = dbuf + d * 2048;
+        const int o = 16 * j + g;
+        db[(2 * t) * 128 + o] = d0[0];
+        db[(2 * t + 1) * 128 + o] = d0[1];
+        db[(2 * t) * 128 + o + 8] = d0[2];
+        db[(2 * t + 1) * 128 + o + 8] = d0[3];
+        db[(2 * t + 8) * 128 + o] = d1[0];
+        db[(2 * t + 9) * 128 + o] = d1[1];
+        db[(2 * t + 8) * 128 + o + 8] = d1[2];
+        db[(2 * t + 9) * 128 + o + 8] = d1[3];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          d0[q] = 0.f;
+          d1[q] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dfull_bar(d));
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int t = threadIdx.x;  // output within the block
+    LinearPass lp;
+    lp.svh = p.svh;
+    lp.y = p.y;
+    lp.out_f32 = p.out_f32;
+    lp.rows = p.rows;
+    lp.in_features = p.in_features;
+    lp.out_features = p.out_features;
+    for (long long bb = b_first; bb <= b_last; ++bb) {
+      const int b = static_cast<int>(bb);
+      const int sg = static_cast<int>(bb - b_first);
+      const int d = sg & 1;
+      const bool ok = mbar_wait(dfull_bar(d), (sg >> 1) & 1, abort_flag);
+      if (!group_all(1, 128, ok)) break;  // the group's named barriers need all 128 threads
+      float v[16];
+      const float* db = dbuf + d * 2048;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) v[r] = db[r * 128 + t];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty_bar(d));
+      const int c_first = cta_of_unit(static_cast<long long>(b) * UB, p.units, p.ctas);
+      const int c_last = cta_of_unit(static_cast<long long>(b + 1) * UB - 1, p.units, p.ctas);
+      if (c_first == c_last) {
+        block_epilogue(v, lp, b, t, xch, 1, 128);
+        continue;
+      }
+      // Block shared with other CTAs: publish the partial sums, count arrivals.
+      float* mine = p.partials + (static_cast<size_t>(c) * 2 + partial_slot(c, b, p)) * 16 * 128;
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (r < p.rows) mine[r * 128 + t] = v[r];
+      __threadfence();
+      group_sync(1, 128);
+      if (t == 0) {
+        const int old = atomicAdd(p.counters + b, 1);
+        *last_flag = (old == c_last - c_first) ? 1 : 0;
+      }
+      group_sync(1, 128);
+      const bool last = *last_flag != 0;
+      if (last) {
+        __threadfence();
+        for (int cc = c_first; cc <= c_last; ++cc) {
+          const float* src =
+              p.partials + (static_cast<size_t>(cc) * 2 + partial_slot(cc, b, p)) * 16 * 128;
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            if (r < p.rows) {
+              const float x = __ldcg(src + r * 128 + t);
+              v[r] = (cc == c_first) ? x : __fadd_rn(v[r], x);
+            }
+          }
+        }
+        block_epilogue(v, lp, b, t, xch, 1, 128);
+        if (t == 0) p.counters[b] = 0;
+      }
+      group_sync(1, 128);
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err_flag, 1);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+template <int BITS, bool TWO>
+cudaError_t set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, TWO>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS>::kBytes);
+  });
+  return err;
+}
+
+template <int BITS>
+cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, cudaStream_t stream) {
+  using L = Layout<BITS>;
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap wmap, xmap;
+  {
+    // Packed weights as rows of u64: one row per k-tile, O * BITS / 4 words.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
+                                static_cast<cuuint64_t>(lp.in_features / 16)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.out_features) * BITS * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(kUnitKt)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(lp.trellis), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // xr [rows][in] fp16; a box of 64 inputs x 16 rows lands as 16 rows of
+    // 128 bytes with the 128-byte swizzle; rows past `rows` are zero.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.in_features), static_cast<cuuint64_t>(lp.rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.in_features) * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(lp.xr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  MmaParams p;
+  p.svh = lp.svh;
+  p.y = lp.y;
+  p.partials = ws.partials;
+  p.counters = ws.counters;
+  p.err_flag = ws.err_flag;
+  p.units_per_block = lp.in_features / 128;
+  p.units = static_cast<long long>(lp.out_features / 128) * p.units_per_block;
+  p.ctas = ws.ctas;
+  p.out_f32 = lp.out_f32;
+  p.rows = lp.rows;
+  p.in_features = lp.in_features;
+  p.out_features = lp.out_features;
+  cudaError_t e;
+  if (lp.rows > 8) {
+    e = set_smem_attr<BITS, true>();
+    if (e != cudaSuccess) return e;
+    trellis_linear_mma_kernel<BITS, true><<<ws.ctas, kThreads, L::kBytes, stream>>>(wmap, xmap, p);
+  } else {
+    e = set_smem_attr<BITS, false>();
+    if (e != cudaSuccess) return e;
+    trellis_linear_mma_kernel<BITS, false><<<ws.ctas, kThreads, L::kBytes, stream>>>(wmap, xmap, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features) {
+  const long long units = static_cast<long long>(out_features / 128) * (in_features / 128);
+  return static_cast<int>(units < num_sms ? units : num_sms);
+}
+
+cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream) {
+  switch (p.bits) {
+    case 2: return run_mma<2>(p, ws, stream);
+    case 3: return run_mma<3>(p, ws, stream);
+    case 4: return run_mma<4>(p, ws, stream);
+    case 5: return run_mma<5>(p, ws, stream);
+    case 6: return run_mma<6>(p, ws, stream);
+    case 8: return run_mma<8>(p, ws, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tfx
