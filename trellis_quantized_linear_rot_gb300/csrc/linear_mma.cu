@@ -28,10 +28,13 @@
 // Warp roles:
 //   warps 0-3   epilogue: sums of a finished segment (from shared memory) ->
 //               output rotation -> svh -> y, or the cross-CTA partial sums
-//   warps 4-11  compute: warp 4 + j owns output tile j (outputs 16j..16j+15 of
-//               the block); per unit it decodes its 8 tiles (one per k-tile)
-//               into A fragments and issues one mma.sync per 8 rows per tile
-//   warp 12     producer: one thread issues the TMA copies of each unit
+//   warps 4-19  compute, two groups of 8: warp 4 + 8q + j of group q owns output
+//               tile j (outputs 16j..16j+15 of the block); group q takes the
+//               units q, q + 2, ... of each segment; per unit a warp decodes its
+//               8 tiles (one per k-tile) into A fragments and issues one
+//               mma.sync per 8 rows per tile; a segment's sum is group 0's
+//               plus group 1's, added in that order
+//   warp 20     producer: one thread issues the TMA copies of each unit
 //               (packed weights of 8 k-tiles x 8 tiles; the 16 x 128 slice of
 //               xr, 128-byte swizzled so the B-fragment loads hit distinct
 //               banks)
@@ -53,15 +56,18 @@ namespace {
 
 constexpr int kUnitKt = 8;           // k-tiles per unit (128 inputs)
 constexpr int kXrUnitBytes = 4096;   // 16 rows x 128 inputs fp16 (two 64-input halves)
-constexpr int kComputeWarps = 8;     // one per 16-output tile of a block
+constexpr int kTileWarps = 8;        // one per 16-output tile of a block
+constexpr int kGroups = 2;           // compute groups of 8 warps, alternating units
+constexpr int kComputeWarps = kTileWarps * kGroups;
 constexpr int kThreads = (4 + kComputeWarps + 1) * 32;
 constexpr int kSmemBudget = 196 * 1024;
+constexpr int kDbufBytes = 2 * kGroups * 16 * 128 * 4;  // per segment buffer and group
 
 template <int BITS>
 struct Cfg {
   static constexpr int kWUnitBytes = 2048 * BITS;  // 8 k-tiles x 8 tiles x 32*BITS bytes
   static constexpr int kStageBytes = kWUnitBytes + kXrUnitBytes;
-  static constexpr int kStagesFit = (kSmemBudget - 3 * 8192 - 1024) / kStageBytes;
+  static constexpr int kStagesFit = (kSmemBudget - kDbufBytes - 8192 - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit < 12 ? kStagesFit : 12;
 };
 
@@ -100,8 +106,8 @@ template <int BITS>
 struct Layout {
   static constexpr int kStages = Cfg<BITS>::kStages;
   static constexpr int kStageBytes = Cfg<BITS>::kStageBytes;
-  static constexpr int kDbufOff = kStages * kStageBytes;        // 2 x [16][128] fp32 segment sums
-  static constexpr int kXchOff = kDbufOff + 2 * 8192;            // [16][128] fp32 for the rotation
+  static constexpr int kDbufOff = kStages * kStageBytes;        // [2][groups][16][128] fp32 sums
+  static constexpr int kXchOff = kDbufOff + kDbufBytes;          // [16][128] fp32 for the rotation
   static constexpr int kBarOff = kXchOff + 8192;
   static constexpr int kNumBars = 2 * kStages + 4;               // full, empty, dfull[2], dempty[2]
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -147,13 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int UB = p.units_per_block;
   const long long b_first = u0 / UB;
   const long long b_last = (u1 - 1) / UB;
+  const int ub_first = static_cast<int>(u0 - b_first * UB);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     *last_flag = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kComputeWarps);
+      mbar_init(empty_bar(s), kTileWarps);  // the 8 warps of the group that takes the unit
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(dfull_bar(d), kComputeWarps);
@@ -171,20 +178,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
+      int b = static_cast<int>(b_first);
+      int ub = ub_first;
+      int s = 0;
+      int round = 0;
       for (int i = 0; i < n_units; ++i) {
-        const int s = i % S;
-        const int k = i / S;
-        if (k > 0 && !mbar_wait(empty_bar(s), (k - 1) & 1, abort_flag)) break;
-        const long long u = u0 + i;
-        const int b = static_cast<int>(u / UB);
-        const int ub = static_cast<int>(u % UB);
+        if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, abort_flag)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
-        const uint32_t xs = st + Cfg<BITS>::kWUnitBytes;
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
         tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(s));
-        tma_load_2d(xs, &xmap, ub * 128, 0, full_bar(s));
-        tma_load_2d(xs + 2048, &xmap, ub * 128 + 64, 0, full_bar(s));
+        tma_load_3d(st + Cfg<BITS>::kWUnitBytes, &xmap, 0, 0, ub * 2, full_bar(s));
         issued = i + 1;
+        if (++ub == UB) {
+          ub = 0;
+          ++b;
+        }
+        if (++s == S) {
+          s = 0;
+          ++round;
+        }
       }
       // Let every copy this CTA started land before it can exit.
       for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
@@ -194,65 +206,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------- compute
-    const int j = warp - 4;   // output tile of the block
-    const int g = lane >> 2;  // outputs g and g + 8 of the tile
-    const int t = lane & 3;   // inputs 4t .. 4t+3 of each k-tile
-    float d0[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 0..7
-    float d1[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 8..15
-    for (int i = 0; i < n_units; ++i) {
-      const long long u = u0 + i;
-      const int ub = static_cast<int>(u % UB);
-      const bool seg_last = (i == n_units - 1) || ub == UB - 1;
-      const int s = i % S;
-      const bool ok = mbar_wait(full_bar(s), (i / S) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const uint8_t* st = smem + s * L::kStageBytes;
-      const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
-      const uint8_t* xs = st + Cfg<BITS>::kWUnitBytes;
-#pragma unroll
-      for (int kt = 0; kt < kUnitKt; ++kt) {
-        const uint32_t* tw = wtile + kt * 64 * BITS;
-        uint32_t a[4];
-        decode_group4<BITS>(tw, g, t, a[0], a[2]);
-        decode_group4<BITS>(tw, g + 8, t, a[1], a[3]);
-        // xr row r, inputs 16kt + 4t .. +3: 128-byte swizzled rows, 16-byte
-        // chunk c of row r stored at chunk c ^ (r % 8).
-        const int chunk = 2 * (kt & 3) + (t >> 1);
-        const int off = (kt >> 2) * 2048 + ((chunk ^ g) << 4) + (t & 1) * 8;
-        const uint2 b_lo = *reinterpret_cast<const uint2*>(xs + off + g * 128);
-        mma_16816(d0, a, b_lo.x, b_lo.y);
-        if (TWO_HALVES) {
-          const uint2 b_hi = *reinterpret_cast<const uint2*>(xs + off + (g + 8) * 128);
-          mma_16816(d1, a, b_hi.x, b_hi.y);
+    const int cg = (warp - 4) / kTileWarps;  // group: takes units cg, cg + kGroups, ... of each segment
+    const int j = (warp - 4) % kTileWarps;   // output tile of the block
+    const int g = lane >> 2;                 // outputs g and g + 8 of the tile
+    const int t = lane & 3;                  // inputs 4t .. 4t+3 of each k-tile
+    bool stop = false;
+    for (long long bb = b_first; bb <= b_last && !stop; ++bb) {
+      const int sg = static_cast<int>(bb - b_first);
+      const long long seg_lo = bb * UB > u0 ? bb * UB - u0 : 0;
+      const long long seg_hi = (bb + 1) * UB - u0 < n_units ? (bb + 1) * UB - u0 : n_units;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 0..7
+      float d1[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 8..15
+      int i = static_cast<int>(seg_lo) + ((cg - static_cast<int>(seg_lo)) % kGroups + kGroups) % kGroups;
+      for (; i < seg_hi; i += kGroups) {
+        const int s = i % S;
+        const bool ok = mbar_wait(full_bar(s), (i / S) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          stop = true;
+          break;
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
-      if (seg_last) {
-        const int sg = static_cast<int>((u / UB) - b_first);
-        const int d = sg & 1;
-        bool ok2 = true;
-        if (sg >= 2) ok2 = mbar_wait(dempty_bar(d), ((sg >> 1) - 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok2)) break;
-        // D fragment: (output g, row 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
-        float* db = dbuf + d * 2048;
-        const int o = 16 * j + g;
-        db[(2 * t) * 128 + o] = d0[0];
-        db[(2 * t + 1) * 128 + o] = d0[1];
-        db[(2 * t) * 128 + o + 8] = d0[2];
-        db[(2 * t + 1) * 128 + o + 8] = d0[3];
-        db[(2 * t + 8) * 128 + o] = d1[0];
-        db[(2 * t + 9) * 128 + o] = d1[1];
-        db[(2 * t + 8) * 128 + o + 8] = d1[2];
-        db[(2 * t + 9) * 128 + o + 8] = d1[3];
+        const uint8_t* st = smem + s * L::kStageBytes;
+        const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
+        const uint8_t* xs = st + Cfg<BITS>::kWUnitBytes;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          d0[q] = 0.f;
-          d1[q] = 0.f;
+        for (int kt = 0; kt < kUnitKt; ++kt) {
+          const uint32_t* tw = wtile + kt * 64 * BITS;
+          uint32_t a[4];
+          decode_group4<BITS>(tw, g, t, a[0], a[2]);
+          decode_group4<BITS>(tw, g + 8, t, a[1], a[3]);
+          // xr row r, inputs 16kt + 4t .. +3: 128-byte swizzled rows, 16-byte
+          // chunk c of row r stored at chunk c ^ (r % 8).
+          const int chunk = 2 * (kt & 3) + (t >> 1);
+          const int off = (kt >> 2) * 2048 + ((chunk ^ g) << 4) + (t & 1) * 8;
+          const uint2 b_lo = *reinterpret_cast<const uint2*>(xs + off + g * 128);
+          mma_16816(d0, a, b_lo.x, b_lo.y);
+          if (TWO_HALVES) {
+            const uint2 b_hi = *reinterpret_cast<const uint2*>(xs + off + (g + 8) * 128);
+            mma_16816(d1, a, b_hi.x, b_hi.y);
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(dfull_bar(d));
+        if (lane == 0) mbar_arrive(empty_bar(s));
       }
+      if (stop) break;
+      // This group's sums of the segment (zero if it took none of its units).
+      const int d = sg & 1;
+      bool ok2 = true;
+      if (sg >= 2) ok2 = mbar_wait(dempty_bar(d), ((sg >> 1) - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok2)) break;
+      // D fragment: (output g, row 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+      float* db = dbuf + (d * kGroups + cg) * 2048;
+      const int o = 16 * j + g;
+      db[(2 * t) * 128 + o] = d0[0];
+      db[(2 * t + 1) * 128 + o] = d0[1];
+      db[(2 * t) * 128 + o + 8] = d0[2];
+      db[(2 * t + 1) * 128 + o + 8] = d0[3];
+      db[(2 * t + 8) * 128 + o] = d1[0];
+      db[(2 * t + 9) * 128 + o] = d1[1];
+      db[(2 * t + 8) * 128 + o + 8] = d1[2];
+      db[(2 * t + 9) * 128 + o + 8] = d1[3];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dfull_bar(d));
     }
   } else {
     // ----------------------------------------------------------- epilogue
@@ -271,9 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = mbar_wait(dfull_bar(d), (sg >> 1) & 1, abort_flag);
       if (!group_all(1, 128, ok)) break;  // the group's named barriers need all 128 threads
       float v[16];
-      const float* db = dbuf + d * 2048;
+      const float* db = dbuf + d * kGroups * 2048;
 #pragma unroll
       for (int r = 0; r < 16; ++r) v[r] = db[r * 128 + t];
+#pragma unroll
+      for (int q = 1; q < kGroups; ++q)  // the groups' sums, added in group order
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = __fadd_rn(v[r], db[q * 2048 + r * 128 + t]);
       __syncwarp();
       if (lane == 0) mbar_arrive(dempty_bar(d));
       const int c_first = cta_of_unit(static_cast<long long>(b) * UB, p.units, p.ctas);
@@ -364,13 +382,15 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, cudaStream_t st
       return cudaErrorInvalidValue;
   }
   {
-    // xr [rows][in] fp16; a box of 64 inputs x 16 rows lands as 16 rows of
-    // 128 bytes with the 128-byte swizzle; rows past `rows` are zero.
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.in_features), static_cast<cuuint64_t>(lp.rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.in_features) * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(lp.xr), dims, strides, box,
+    // xr [rows][in] fp16 viewed as (64 inputs, rows, in / 64): a box of
+    // (64, 16, 2) lands as two 64-input halves of 16 rows of 128 bytes each,
+    // with the 128-byte swizzle; rows past `rows` are zero.
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows),
+                                static_cast<cuuint64_t>(lp.in_features / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};
+    const cuuint32_t box[3] = {64, 16, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
