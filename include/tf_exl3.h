@@ -42,7 +42,8 @@ typedef enum {
   TF_ERR_ALIGN = 5,    /* a pointer is not 16-byte aligned                     */
   TF_ERR_CUDA = 6,     /* a CUDA runtime call or launch failed (tf_last_error) */
   TF_ERR_TIMEOUT = 7,  /* a kernel's bounded wait expired (tf_device_error)    */
-  TF_ERR_POINTER = 8   /* a pointer is not device memory of the current device */
+  TF_ERR_POINTER = 8,  /* a pointer is not device memory of the current device */
+  TF_ERR_SCRATCH = 9   /* the problem needs more scratch than tf_trellis_linear_noalloc holds */
 } tf_status;
 
 typedef enum { TF_F16 = 0, TF_F32 = 1, TF_BF16 = 2 } tf_dtype;
@@ -99,6 +100,29 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
 tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh,
                             void* y, int out_dtype, int rows, int in_features,
                             int out_features, int bits, void* stream);
+
+/*
+ * tf_trellis_linear_noalloc -- the same computation as tf_trellis_linear
+ * (same arguments, layouts, results and refusals) for callers that must not
+ * let a library allocate device memory: for example a serving process whose
+ * caching allocator has already reserved the memory it plans around, where
+ * a cudaMalloc can fail or break that plan, or code that cannot accept the
+ * implicit device synchronisation cudaMalloc and cudaFree may cause. The
+ * pages describe no counterpart; this is an addition of this library.
+ * Its scratch (partial sums of output blocks shared by two thread blocks and
+ * one arrival counter per output block) lives in a fixed device array of
+ * about 2.6 MB that every GPU loading this library holds until the process
+ * exits. Limits: out_features <= 2,097,152 (16,384 blocks of 128), else
+ * TF_ERR_SCRATCH; at most 160 thread blocks per launch. The first call on a
+ * device looks up the array's device address on that device (call it once
+ * before capturing work into a CUDA graph). Each call clears the counters it
+ * uses with cudaMemsetAsync on `stream`. All calls share the one array, so
+ * calls whose work overlaps on the GPU (for example on two streams) race and
+ * must be ordered by the caller. Calls no cudaMalloc or cudaFree.
+ */
+tf_status tf_trellis_linear_noalloc(const void* xr, const void* trellis, const void* svh,
+                                    void* y, int out_dtype, int rows, int in_features,
+                                    int out_features, int bits, void* stream);
 
 /*
  * tf_trellis_decode -- the weights alone: writes the dense fp16 matrix

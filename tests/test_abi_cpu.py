@@ -43,7 +43,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.tf_abi_version() == 1
-    for s in range(9):
+    for s in range(10):
         assert lib.tf_status_string(s).decode() not in ("", "unknown status")
     assert lib.tf_status_string(99).decode() == "unknown status"
 

@@ -1,0 +1,64 @@
+"""The allocation-free entry point, tf_trellis_linear_noalloc, against the
+regular one, through the C ABI on the GPU.
+
+It exists for callers that cannot let the library call cudaMalloc: for
+example a serving process whose caching allocator already holds the device
+memory it plans around, or code that must not risk the implicit device
+synchronisation an allocation can cause. Its scratch lives in a fixed device
+array instead. This file is collected last, so a run that stops at the first
+failure has already run every other test; it must also pass on its own in a
+fresh process.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+from oracle import exl3 as o
+from trellis_quantized_linear_rot_gb300 import synth
+from helpers import assert_close_f32, dev, host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import trellis_quantized_linear_rot_gb300 as tf  # noqa: E402
+
+
+def _call_noalloc(xr_t, tr_t, svh_t, y_t, bits, rows, i_f, o_f):
+    lib = tf.lib()
+    return lib.tf_trellis_linear_noalloc(
+        ctypes.c_void_p(xr_t.data_ptr()), ctypes.c_void_p(tr_t.data_ptr()),
+        ctypes.c_void_p(svh_t.data_ptr()), ctypes.c_void_p(y_t.data_ptr()),
+        tf.TF_F32 if y_t.dtype == torch.float32 else tf.TF_F16, rows, i_f, o_f, bits,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("i_f,o_f,bits,rows", [(6144, 25600, 4, 16), (5120, 129280, 4, 1), (384, 256, 6, 17)])
+def test_noalloc_matches_regular_entry_point_twice(i_f, o_f, bits, rows):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    x = synth.make_x(rows, i_f, 901)
+    suh = synth.make_scale(i_f, 902)
+    svh = synth.make_scale(o_f, 903)
+    tr = synth.make_trellis(i_f, o_f, bits, 904)
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    tr_t, svh_t = dev(tr), dev(svh)
+    want = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32))
+    for _ in range(2):                       # two calls in a row share the array
+        y_t = torch.full((rows, o_f), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call_noalloc(xr_t, tr_t, svh_t, y_t, bits, rows, i_f, o_f) == tf.TF_OK
+        tf.tf_device_error()
+        got = host(y_t)
+        assert_close_f32(got, want.astype(np.float64), tol=1e-6)
+    blocks = [0, o_f // 128 - 1]
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(host(xr_t), o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f32(got[:, cols], ref)
+
+
+def test_noalloc_refuses_more_outputs_than_its_array_holds():
+    lib = tf.lib()
+    p = ctypes.c_void_p(0x10000)
+    st = lib.tf_trellis_linear_noalloc(p, p, p, p, tf.TF_F32, 1, 512, 128 * 20000, 4, ctypes.c_void_p(0))
+    assert st == tf.TF_ERR_SCRATCH

@@ -15,7 +15,7 @@ import os
 from . import build as _build
 
 TF_OK, TF_ERR_NULL, TF_ERR_SHAPE, TF_ERR_BITS, TF_ERR_DTYPE = 0, 1, 2, 3, 4
-TF_ERR_ALIGN, TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_POINTER = 5, 6, 7, 8
+TF_ERR_ALIGN, TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_POINTER, TF_ERR_SCRATCH = 5, 6, 7, 8, 9
 TF_F16, TF_F32, TF_BF16 = 0, 1, 2
 
 # Every entry point include/tf_exl3.h declares, with its ctypes signature.
@@ -24,6 +24,7 @@ SIGNATURES = {
     "tf_abi_version": (_I, []),
     "tf_rot_in": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP]),
     "tf_trellis_linear": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tf_trellis_linear_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_decode": (_I, [_VP, _VP, _I, _I, _I, _VP]),
     "tf_trellis_bytes": (_SZ, [_I, _I, _I]),
     "tf_status_string": (ctypes.c_char_p, [_I]),

@@ -121,6 +121,23 @@ tf_status check_device_ptrs(int device, P... ptrs) {
 }
 
 }  // namespace
+
+tf_status current_device_state(int* device, int* num_sms, int** err_flag) {
+  DeviceCtx* ctx = nullptr;
+  tf_status s = current_ctx(&ctx);
+  if (s != TF_OK) return s;
+  *device = ctx->device;
+  *num_sms = ctx->num_sms;
+  *err_flag = ctx->err_flag;
+  return TF_OK;
+}
+
+tf_status check_pointers_on_device(int device, const void* a, const void* b, const void* c, const void* d) {
+  return check_device_ptrs(device, a, b, c, d);
+}
+
+tf_status record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
 }  // namespace tfx
 
 using namespace tfx;
@@ -140,6 +157,7 @@ const char* tf_status_string(int status) {
     case TF_ERR_CUDA: return "a CUDA call failed (see tf_last_error)";
     case TF_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     case TF_ERR_POINTER: return "a pointer is not device memory of the current device";
+    case TF_ERR_SCRATCH: return "the problem needs more scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }

@@ -6,7 +6,14 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "tf_exl3.h"
+
 namespace tfx {
+
+// Host helpers of the C ABI (api.cu) for entry points in other files.
+tf_status current_device_state(int* device, int* num_sms, int** err_flag);
+tf_status check_pointers_on_device(int device, const void* a, const void* b, const void* c, const void* d);
+tf_status record_cuda_error(cudaError_t e, const char* what);
 
 cudaError_t launch_rot_in(const void* x, int x_dtype, const __half* suh, __half* xr, int rows,
                           int in_features, int num_sms, cudaStream_t stream);
