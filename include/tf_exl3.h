@@ -102,6 +102,29 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
                             int out_features, int bits, void* stream);
 
 /*
+ * tf_trellis_linear_strips -- tf_trellis_linear on the same tiles stored in
+ * the "strips" order ("Checks on this head": the decode test runs on the
+ * checkpoint's tile layout and on the strips layout). A strip is one block of
+ * 128 outputs stored whole: for block b < out/128 and unit u < in/128, the 64
+ * tiles (kt = 8u + kk, nt = 8b + nn) follow at word
+ * ((b * in/128 + u) * 64 + kk * 8 + nn) * 8 * bits, each tile's 8*bits words
+ * unchanged. Each 128-input unit of a block is then one contiguous run,
+ * which the GPU streams at a higher rate than the k-tile-major order.
+ * Same arguments, results (bit for bit) and refusals as tf_trellis_linear.
+ */
+tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const void* svh,
+                                   void* y, int out_dtype, int rows, int in_features,
+                                   int out_features, int bits, void* stream);
+
+/*
+ * tf_trellis_to_strips -- repacks tiles from the k-tile-major order of
+ * tf_trellis_linear into the strips order of tf_trellis_linear_strips
+ * (tf_trellis_bytes(in, out, bits) bytes each; the buffers must not overlap).
+ */
+tf_status tf_trellis_to_strips(const void* tiles, void* strips, int in_features,
+                               int out_features, int bits, void* stream);
+
+/*
  * tf_trellis_linear_noalloc -- the same computation as tf_trellis_linear
  * (same arguments, layouts, results and refusals) for callers that must not
  * let a library allocate device memory: for example a serving process whose

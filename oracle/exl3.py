@@ -288,3 +288,26 @@ def decode_rows(trellis, in_features, out_features, bits, ks):
         w = decode_tiles(t[k // 16], bits)               # [nt, 16k, 16n]
         out.append(w[:, k % 16, :].reshape(out_features))
     return np.stack(out)
+
+
+# ---------------------------------------------------------------------------
+# The second storage order of the same tiles ("Checks on this head": the
+# decode test runs on the checkpoint's tile layout and on the strips layout).
+# Reading: a strip is one block of 128 outputs; it is stored whole, unit by
+# unit (128 inputs = 8 k-tiles), each unit's 64 tiles in [k-tile][n-tile]
+# order. The tiles themselves (their 8*bits words) are unchanged.
+# ---------------------------------------------------------------------------
+def tiles_to_strips(trellis, in_features, out_features, bits):
+    """k-tile-major packed tiles -> strips order (same words, other order)."""
+    check_shape(in_features, out_features, bits)
+    kt, nt = in_features // 16, out_features // 16
+    t = np.asarray(trellis, dtype=np.uint32).reshape(kt // 8, 8, nt // 8, 8, 8 * bits)
+    # [unit][kt%8][strip][nt%8][words] -> [strip][unit][kt%8][nt%8][words]
+    return np.ascontiguousarray(t.transpose(2, 0, 1, 3, 4)).reshape(-1)
+
+
+def strips_to_tiles(strips, in_features, out_features, bits):
+    check_shape(in_features, out_features, bits)
+    kt, nt = in_features // 16, out_features // 16
+    s = np.asarray(strips, dtype=np.uint32).reshape(nt // 8, kt // 8, 8, 8, 8 * bits)
+    return np.ascontiguousarray(s.transpose(1, 2, 0, 3, 4)).reshape(-1)

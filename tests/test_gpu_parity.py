@@ -208,6 +208,32 @@ def test_non_finite_classes_match_float64():
     assert np.array_equal(np.isneginf(y), np.isneginf(ref))
 
 
+# ------------------------------------------------------------ strips layout
+@pytest.mark.parametrize("bits", o.BITS_ALLOWED)
+def test_to_strips_matches_oracle_order(bits):
+    i_f, o_f = 384, 256
+    tr = synth.make_trellis(i_f, o_f, bits, 800 + bits)
+    got = host(tf.tf_trellis_to_strips(dev(tr), i_f, o_f, bits)).view(np.uint32)
+    assert np.array_equal(got, o.tiles_to_strips(tr, i_f, o_f, bits))
+
+
+@pytest.mark.parametrize("bits,rows", [(4, 1), (4, 16), (6, 9), (8, 3), (3, 16), (2, 5), (5, 12)])
+def test_linear_strips_equals_tiles_bit_for_bit(bits, rows):
+    """The strips order streams the same tiles: outputs are identical bits,
+    and match the oracle (sampled) on the wkv shape."""
+    i_f, o_f = 6144, 25600
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=7)
+    xr_t, tr_t, svh_t = dev(o.rot_in_f32(x, suh)), dev(tr), dev(svh)
+    strips_t = tf.tf_trellis_to_strips(tr_t, i_f, o_f, bits)
+    a = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32))
+    b = host(tf.tf_trellis_linear_strips(xr_t, strips_t, svh_t, bits, o_f, out_dtype=torch.float32))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    blocks = [5, 123]
+    cols = np.concatenate([np.arange(128 * bl, 128 * bl + 128) for bl in blocks])
+    ref = o.linear_f64(host(xr_t), o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f32(b[:, cols], ref)
+
+
 # ------------------------------------------------------- GPU-vs-GPU invariants
 def test_row_independence_windows_and_passes():
     """LM head 5120 -> 129,280 at 6 bits, 64 rows as four passes of 16: every

@@ -470,3 +470,18 @@ def test_decode_rows_and_blocks_agree_with_matrix():
     ks = [0, 17, 255]
     assert np.array_equal(bits16(o.decode_rows(tr, 256, 256, k, ks)), bits16(w[ks]))
     assert np.array_equal(bits16(o.decode_blocks(tr, 256, 256, k, [1])), bits16(w[:, 128:]))
+
+
+def test_strips_layout_places_each_tile_by_hand_formula():
+    k, i_f, o_f = 2, 256, 384
+    tr = synth.make_trellis(i_f, o_f, k, 91)
+    st = o.tiles_to_strips(tr, i_f, o_f, k)
+    per = 8 * k
+    ub = i_f // 128
+    for kt in range(i_f // 16):
+        for nt in range(o_f // 16):
+            src = (kt * (o_f // 16) + nt) * per
+            b, u = nt // 8, kt // 8
+            dst = ((b * ub + u) * 64 + (kt % 8) * 8 + nt % 8) * per
+            assert np.array_equal(st[dst:dst + per], tr[src:src + per])
+    assert np.array_equal(o.strips_to_tiles(st, i_f, o_f, k), tr)

@@ -25,6 +25,8 @@ SIGNATURES = {
     "tf_rot_in": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP]),
     "tf_trellis_linear": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tf_trellis_linear_strips": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tf_trellis_to_strips": (_I, [_VP, _VP, _I, _I, _I, _VP]),
     "tf_trellis_decode": (_I, [_VP, _VP, _I, _I, _I, _VP]),
     "tf_trellis_bytes": (_SZ, [_I, _I, _I]),
     "tf_status_string": (ctypes.c_char_p, [_I]),
@@ -144,6 +146,33 @@ def tf_trellis_linear(xr, trellis, svh, bits, out_features, out_dtype=None, y=No
                                  in_f, out_features, bits, _stream(stream))
     _check(st, "tf_trellis_linear")
     return y
+
+
+def tf_trellis_linear_strips(xr, strips, svh, bits, out_features, out_dtype=None, y=None, stream=None):
+    """tf_trellis_linear on weights stored in the strips order (tf_trellis_to_strips)."""
+    import torch
+    rows, in_f = xr.shape
+    for t, n in ((xr, "xr"), (strips, "strips"), (svh, "svh")):
+        _contig(t, n)
+    if y is None:
+        y = torch.empty((rows, out_features), dtype=out_dtype or torch.float32, device=xr.device)
+    _contig(y, "y")
+    st = lib().tf_trellis_linear_strips(_ptr(xr), _ptr(strips), _ptr(svh), _ptr(y), _dtype_code(y.dtype),
+                                        rows, in_f, out_features, bits, _stream(stream))
+    _check(st, "tf_trellis_linear_strips")
+    return y
+
+
+def tf_trellis_to_strips(tiles, in_features, out_features, bits, strips=None, stream=None):
+    """Repacks k-tile-major packed tiles into the strips order."""
+    import torch
+    _contig(tiles, "tiles")
+    if strips is None:
+        strips = torch.empty_like(tiles)
+    st = lib().tf_trellis_to_strips(_ptr(tiles), _ptr(strips), in_features, out_features, bits,
+                                    _stream(stream))
+    _check(st, "tf_trellis_to_strips")
+    return strips
 
 
 def tf_trellis_decode(trellis, in_features, out_features, bits, w=None, stream=None):

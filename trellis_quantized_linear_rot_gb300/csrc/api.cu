@@ -190,9 +190,9 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr, int r
   return TF_OK;
 }
 
-tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh, void* y,
-                            int out_dtype, int rows, int in_features, int out_features, int bits,
-                            void* stream) {
+static tf_status linear_entry(const void* xr, const void* trellis, const void* svh, void* y,
+                              int out_dtype, int rows, int in_features, int out_features, int bits,
+                              bool strips, void* stream) {
   if (rows < 0 || !valid_features(in_features, kMaxInFeatures) ||
       !valid_features(out_features, kMaxOutFeatures))
     return TF_ERR_SHAPE;
@@ -225,9 +225,41 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
     p.in_features = in_features;
     p.out_features = out_features;
     p.bits = bits;
-    cudaError_t e = launch_trellis_linear_mma(p, ws, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_trellis_linear_mma(p, ws, strips, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "trellis linear launch");
   }
+  return TF_OK;
+}
+
+tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh, void* y,
+                            int out_dtype, int rows, int in_features, int out_features, int bits,
+                            void* stream) {
+  return linear_entry(xr, trellis, svh, y, out_dtype, rows, in_features, out_features, bits, false,
+                      stream);
+}
+
+tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const void* svh, void* y,
+                                   int out_dtype, int rows, int in_features, int out_features,
+                                   int bits, void* stream) {
+  return linear_entry(xr, strips, svh, y, out_dtype, rows, in_features, out_features, bits, true,
+                      stream);
+}
+
+tf_status tf_trellis_to_strips(const void* tiles, void* strips, int in_features, int out_features,
+                               int bits, void* stream) {
+  if (!valid_features(in_features, kMaxInFeatures) || !valid_features(out_features, kMaxOutFeatures))
+    return TF_ERR_SHAPE;
+  if (!valid_bits(bits)) return TF_ERR_BITS;
+  if (!tiles || !strips) return TF_ERR_NULL;
+  if (!aligned16(tiles) || !aligned16(strips)) return TF_ERR_ALIGN;
+  DeviceCtx* ctx = nullptr;
+  tf_status s = current_ctx(&ctx);
+  if (s != TF_OK) return s;
+  s = check_device_ptrs(ctx->device, tiles, strips);
+  if (s != TF_OK) return s;
+  cudaError_t e = launch_tiles_to_strips(static_cast<const uint32_t*>(tiles), static_cast<uint32_t*>(strips),
+                                         in_features, out_features, bits, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tiles-to-strips launch");
   return TF_OK;
 }
 

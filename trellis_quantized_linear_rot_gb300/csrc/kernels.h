@@ -57,6 +57,10 @@ struct TcWorkspace {
 };
 
 int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features);
-cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream);
+// strips = false: packed tiles in k-tile-major order; true: strips order.
+cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
+                                      cudaStream_t stream);
+cudaError_t launch_tiles_to_strips(const uint32_t* tiles, uint32_t* strips, int in_features,
+                                   int out_features, int bits, cudaStream_t stream);
 
 }  // namespace tfx

@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "decode.cuh"
@@ -72,6 +73,7 @@ struct Cfg {
 };
 
 struct MmaParams {
+  const uint8_t* strips;  // packed weights in strips order (strips layout only)
   const __half* svh;
   void* y;
   float* partials;      // [ctas][2][16][128]
@@ -124,7 +126,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int BITS, bool TWO_HALVES>
+// Weight layouts: k-tile major ("tiles": tile (kt, nt) at (kt*O/16 + nt)),
+// or block-contiguous ("strips": block b, unit u, then [kt % 8][nt % 8]).
+// Either way a unit lands in shared memory as [8 k-tiles][8 tiles].
+enum { kLayoutTiles = 0, kLayoutStrips = 1 };
+
+template <int BITS, bool TWO_HALVES, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1)
     trellis_linear_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                               const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&wmap);
+    if (LAYOUT == kLayoutTiles) tma_prefetch_desc(&wmap);
     tma_prefetch_desc(&xmap);
   }
   __syncthreads();
@@ -182,11 +189,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ub = ub_first;
       int s = 0;
       int round = 0;
-      for (int i = 0; i < n_units; ++i) {
+      // The first stages' weight copies need nothing from the kernel before
+      // this one (the rotation that writes xr); the xr copies wait for it.
+      const int pre = n_units < S ? n_units : S;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = smem_u32(smem + i * L::kStageBytes);
+        mbar_arrive_expect_tx(full_bar(i), L::kStageBytes);
+        if (LAYOUT == kLayoutTiles)
+          tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(i));
+        else
+          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * Cfg<BITS>::kWUnitBytes,
+                       Cfg<BITS>::kWUnitBytes, full_bar(i));
+        if (++ub == UB) {
+          ub = 0;
+          ++b;
+        }
+      }
+      pdl_wait_prerequisites();
+      ub = ub_first;
+      for (int i = 0; i < pre; ++i) {
+        tma_load_3d(smem_u32(smem + i * L::kStageBytes) + Cfg<BITS>::kWUnitBytes, &xmap, 0, 0, ub * 2,
+                    full_bar(i));
+        if (++ub == UB) ub = 0;
+      }
+      issued = pre;
+      s = pre == S ? 0 : pre;
+      round = pre == S ? 1 : 0;
+      for (int i = pre; i < n_units; ++i) {
         if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, abort_flag)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
-        tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(s));
+        if (LAYOUT == kLayoutTiles)
+          tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(s));
+        else
+          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * Cfg<BITS>::kWUnitBytes,
+                       Cfg<BITS>::kWUnitBytes, full_bar(s));
         tma_load_3d(st + Cfg<BITS>::kWUnitBytes, &xmap, 0, 0, ub * 2, full_bar(s));
         issued = i + 1;
         if (++ub == UB) {
@@ -210,6 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = (warp - 4) % kTileWarps;   // output tile of the block
     const int g = lane >> 2;                 // outputs g and g + 8 of the tile
     const int t = lane & 3;                  // inputs 4t .. 4t+3 of each k-tile
+    // Byte offsets of this lane's B fragments inside a unit's xr slice, for
+    // k-tiles kt % 4 = 0..3 (row g; row g + 8 is 1024 bytes further): 16-byte
+    // chunk c = 2 (kt % 4) + t / 2 of a 128-byte row sits at chunk c ^ (row % 8).
+    int xoff[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xoff[q] = g * 128 + (((2 * q + (t >> 1)) ^ g) << 4) + (t & 1) * 8;
     bool stop = false;
     for (long long bb = b_first; bb <= b_last && !stop; ++bb) {
       const int sg = static_cast<int>(bb - b_first);
@@ -234,14 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t a[4];
           decode_group4<BITS>(tw, g, t, a[0], a[2]);
           decode_group4<BITS>(tw, g + 8, t, a[1], a[3]);
-          // xr row r, inputs 16kt + 4t .. +3: 128-byte swizzled rows, 16-byte
-          // chunk c of row r stored at chunk c ^ (r % 8).
-          const int chunk = 2 * (kt & 3) + (t >> 1);
-          const int off = (kt >> 2) * 2048 + ((chunk ^ g) << 4) + (t & 1) * 8;
-          const uint2 b_lo = *reinterpret_cast<const uint2*>(xs + off + g * 128);
+          // xr rows g and g + 8, inputs 16kt + 4t .. +3.
+          const uint8_t* xb = xs + (kt >> 2) * 2048 + xoff[kt & 3];
+          const uint2 b_lo = *reinterpret_cast<const uint2*>(xb);
           mma_16816(d0, a, b_lo.x, b_lo.y);
           if (TWO_HALVES) {
-            const uint2 b_hi = *reinterpret_cast<const uint2*>(xs + off + (g + 8) * 128);
+            const uint2 b_hi = *reinterpret_cast<const uint2*>(xb + 1024);
             mma_16816(d1, a, b_hi.x, b_hi.y);
           }
         }
@@ -352,24 +393,52 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, bool TWO>
+template <int BITS, bool TWO, int LAYOUT>
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, TWO>,
+    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, TWO, LAYOUT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS>::kBytes);
   });
   return err;
 }
 
+template <int BITS, bool TWO, int LAYOUT>
+cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
+                       cudaStream_t stream) {
+  cudaError_t e = set_smem_attr<BITS, TWO, LAYOUT>();
+  if (e != cudaSuccess) return e;
+  // Programmatic stream serialisation: this kernel may start while the
+  // kernel before it (the input rotation) finishes; its producer waits for
+  // that kernel's writes before it copies xr.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<BITS>::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, trellis_linear_mma_kernel<BITS, TWO, LAYOUT>, wmap, xmap, p);
+}
+
+template <int BITS, int LAYOUT>
+cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
+                       cudaStream_t stream) {
+  return p.rows > 8 ? launch_one<BITS, true, LAYOUT>(wmap, xmap, p, ctas, stream)
+                    : launch_one<BITS, false, LAYOUT>(wmap, xmap, p, ctas, stream);
+}
+
 template <int BITS>
-cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, cudaStream_t stream) {
-  using L = Layout<BITS>;
+cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap wmap, xmap;
-  {
+  memset(&wmap, 0, sizeof(wmap));
+  if (!strips) {
     // Packed weights as rows of u64: one row per k-tile, O * BITS / 4 words.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
                                 static_cast<cuuint64_t>(lp.in_features / 16)};
@@ -396,6 +465,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, cudaStream_t st
       return cudaErrorInvalidValue;
   }
   MmaParams p;
+  p.strips = reinterpret_cast<const uint8_t*>(lp.trellis);
   p.svh = lp.svh;
   p.y = lp.y;
   p.partials = ws.partials;
@@ -408,17 +478,8 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, cudaStream_t st
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
-  cudaError_t e;
-  if (lp.rows > 8) {
-    e = set_smem_attr<BITS, true>();
-    if (e != cudaSuccess) return e;
-    trellis_linear_mma_kernel<BITS, true><<<ws.ctas, kThreads, L::kBytes, stream>>>(wmap, xmap, p);
-  } else {
-    e = set_smem_attr<BITS, false>();
-    if (e != cudaSuccess) return e;
-    trellis_linear_mma_kernel<BITS, false><<<ws.ctas, kThreads, L::kBytes, stream>>>(wmap, xmap, p);
-  }
-  return cudaGetLastError();
+  return strips ? launch_mma<BITS, kLayoutStrips>(wmap, xmap, p, ws.ctas, stream)
+                : launch_mma<BITS, kLayoutTiles>(wmap, xmap, p, ws.ctas, stream);
 }
 
 }  // namespace
@@ -428,14 +489,15 @@ int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features) {
   return static_cast<int>(units < num_sms ? units : num_sms);
 }
 
-cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, cudaStream_t stream) {
+cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
+                                      cudaStream_t stream) {
   switch (p.bits) {
-    case 2: return run_mma<2>(p, ws, stream);
-    case 3: return run_mma<3>(p, ws, stream);
-    case 4: return run_mma<4>(p, ws, stream);
-    case 5: return run_mma<5>(p, ws, stream);
-    case 6: return run_mma<6>(p, ws, stream);
-    case 8: return run_mma<8>(p, ws, stream);
+    case 2: return run_mma<2>(p, ws, strips, stream);
+    case 3: return run_mma<3>(p, ws, strips, stream);
+    case 4: return run_mma<4>(p, ws, strips, stream);
+    case 5: return run_mma<5>(p, ws, strips, stream);
+    case 6: return run_mma<6>(p, ws, strips, stream);
+    case 8: return run_mma<8>(p, ws, strips, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -105,7 +105,7 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
     p.in_features = in_features;
     p.out_features = out_features;
     p.bits = bits;
-    e = launch_trellis_linear_mma(p, ws, st);
+    e = launch_trellis_linear_mma(p, ws, false, st);
     if (e != cudaSuccess) return record_cuda_error(e, "trellis linear (no-alloc) launch");
   }
   return TF_OK;

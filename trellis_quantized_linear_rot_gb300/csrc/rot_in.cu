@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace tfx {
 
@@ -54,6 +55,9 @@ __global__ void __launch_bounds__(256) rot_in_kernel(const void* __restrict__ x,
                                                      const __half* __restrict__ suh,
                                                      __half* __restrict__ xr, int rows,
                                                      int in_features) {
+  // The linear that follows may start its prologue (its weight copies need
+  // nothing from this kernel); it waits for xr before reading it.
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int warps_per_cta = blockDim.x >> 5;
   const int blocks_per_row = in_features >> 7;

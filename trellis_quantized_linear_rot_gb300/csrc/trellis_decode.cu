@@ -35,6 +35,28 @@ __global__ void __launch_bounds__(128) trellis_decode_kernel(const uint32_t* __r
   }
 }
 
+// Tiles -> strips: one 16-byte chunk per thread, written in strips order.
+// Strips order: block b of 128 outputs, then unit u of 128 inputs, then
+// [k-tile % 8][n-tile % 8], each tile's 8*bits words unchanged.
+__global__ void __launch_bounds__(256) tiles_to_strips_kernel(const uint4* __restrict__ tiles,
+                                                              uint4* __restrict__ strips,
+                                                              long long chunks, int chunks_per_tile,
+                                                              int units_per_block, int n_tiles) {
+  for (long long q = blockIdx.x * 256LL + threadIdx.x; q < chunks; q += static_cast<long long>(gridDim.x) * 256) {
+    const long long td = q / chunks_per_tile;
+    const int within = static_cast<int>(q - td * chunks_per_tile);
+    const long long per_block = static_cast<long long>(units_per_block) * 64;
+    const long long b = td / per_block;
+    const int rem = static_cast<int>(td - b * per_block);
+    const int u = rem >> 6;
+    const int kk = (rem >> 3) & 7;
+    const int nn = rem & 7;
+    const long long kt = 8LL * u + kk;
+    const long long nt = 8LL * b + nn;
+    strips[q] = tiles[(kt * n_tiles + nt) * chunks_per_tile + within];
+  }
+}
+
 template <template <int> class F, typename... Args>
 cudaError_t dispatch_bits(int bits, Args&&... args) {
   switch (bits) {
@@ -59,6 +81,18 @@ struct DecodeLauncher {
 };
 
 }  // namespace
+
+cudaError_t launch_tiles_to_strips(const uint32_t* tiles, uint32_t* strips, int in_features,
+                                   int out_features, int bits, cudaStream_t stream) {
+  const int chunks_per_tile = 2 * bits;  // 8 * bits words = 2 * bits chunks of 16 bytes
+  const long long chunks = static_cast<long long>(in_features / 16) * (out_features / 16) * chunks_per_tile;
+  long long grid = (chunks + 255) / 256;
+  if (grid > 152LL * 16) grid = 152LL * 16;
+  tiles_to_strips_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(tiles), reinterpret_cast<uint4*>(strips), chunks, chunks_per_tile,
+      in_features / 128, out_features / 16);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_trellis_decode(const uint32_t* trellis, __half* w, int in_features,
                                   int out_features, int bits, cudaStream_t stream) {
