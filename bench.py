@@ -229,8 +229,11 @@ def run_ours(args):
     # Inputs (untimed): two copies of the packed weights, x for 16 rows.
     tr_np = synth.make_trellis(IN_F, OUT_F, BITS, synth.SEED_TRELLIS + 2 + BITS)
     tr0 = torch.from_numpy(tr_np.view(np.int32)).to(dev)
-    tr1 = tr0.clone()
     del tr_np
+    if args.layout == "strips":
+        tr0 = tf.tf_trellis_to_strips(tr0, IN_F, OUT_F, BITS)
+    tr1 = tr0.clone()
+    linear = tf.tf_trellis_linear_strips if args.layout == "strips" else tf.tf_trellis_linear
     trs = (tr0, tr1)
     x = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).to(dev)
     suh = torch.from_numpy(synth.make_scale(IN_F, synth.SEED_SUH + 2)).to(dev)
@@ -249,7 +252,7 @@ def run_ours(args):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            tf.tf_trellis_linear(xrs[r], t, svh, BITS, OUT_F, y=ys[r])
+            linear(xrs[r], t, svh, BITS, OUT_F, y=ys[r])
             if record:
                 e1.record(stream)
                 ev[r].append((e0, e1))
@@ -299,7 +302,8 @@ def run_ours(args):
     def e2e_step():
         for r in ROWS:
             xd = x_host[:r].to(dev, non_blocking=True)
-            y = tf.project(xd, suh, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
+            xr = tf.tf_rot_in(xd, suh)
+            y = linear(xr, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
             call[0] += 1
             y_host[r].copy_(y, non_blocking=True)
         torch.cuda.synchronize()
@@ -337,6 +341,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "f16 (fp32 sums)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F, "out_features": OUT_F,
                    "bits": BITS, "out_dtype": "fp32", "weight_bytes_per_call": weight_bytes(),
+                   "layout": args.layout,
                    "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "by_rows": per_rows,
@@ -365,6 +370,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
+    ap.add_argument("--layout", choices=["tiles", "strips"], default="tiles",
+                    help="weight storage order: k-tile major (tiles) or block-contiguous (strips)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

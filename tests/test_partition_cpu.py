@@ -19,11 +19,14 @@ def partial_slot(c, b, units, ctas, ub):
     return 0 if b == range_start(c, units, ctas) // ub else 1
 
 
+@pytest.mark.parametrize("unit_inputs", [128, 256])
 @pytest.mark.parametrize("i_f,o_f,sms", [(5120, 129280, 152), (6144, 25600, 152), (512, 128, 152),
                                          (384, 256, 152), (5120, 129280, 148), (128, 128, 4),
                                          (6144, 128, 152), (1024, 8192, 132)])
-def test_partition_covers_each_unit_once(i_f, o_f, sms):
-    ub = i_f // 128
+def test_partition_covers_each_unit_once(i_f, o_f, sms, unit_inputs):
+    if i_f % unit_inputs:
+        pytest.skip("unit size does not divide the inputs")
+    ub = i_f // unit_inputs
     units = (o_f // 128) * ub
     ctas = min(sms, units)
     owner = {}

@@ -212,7 +212,7 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
   ws.partials = ctx->partials;
   ws.counters = ctx->counters;
   ws.err_flag = ctx->err_flag;
-  ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features);
+  ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
   for (int r0 = 0; r0 < rows; r0 += 16) {
     LinearPass p;

@@ -56,7 +56,7 @@ struct TcWorkspace {
   int ctas;
 };
 
-int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features);
+int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features, int bits);
 // strips = false: packed tiles in k-tile-major order; true: strips order.
 cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
                                       cudaStream_t stream);

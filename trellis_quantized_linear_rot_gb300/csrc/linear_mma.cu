@@ -55,8 +55,6 @@ namespace tfx {
 
 namespace {
 
-constexpr int kUnitKt = 8;           // k-tiles per unit (128 inputs)
-constexpr int kXrUnitBytes = 4096;   // 16 rows x 128 inputs fp16 (two 64-input halves)
 constexpr int kTileWarps = 8;        // one per 16-output tile of a block
 constexpr int kGroups = 2;           // compute groups of 8 warps, alternating units
 constexpr int kComputeWarps = kTileWarps * kGroups;
@@ -64,9 +62,12 @@ constexpr int kThreads = (4 + kComputeWarps + 1) * 32;
 constexpr int kSmemBudget = 196 * 1024;
 constexpr int kDbufBytes = 2 * kGroups * 16 * 128 * 4;  // per segment buffer and group
 
-template <int BITS>
+// A unit is UKT k-tiles (16 * UKT inputs) of one output block: 8, or 16 when
+// the input count allows (fewer synchronisations per weight).
+template <int BITS, int UKT>
 struct Cfg {
-  static constexpr int kWUnitBytes = 2048 * BITS;  // 8 k-tiles x 8 tiles x 32*BITS bytes
+  static constexpr int kWUnitBytes = 256 * BITS * UKT;  // UKT k-tiles x 8 tiles x 32*BITS bytes
+  static constexpr int kXrUnitBytes = 512 * UKT;        // 16 rows x 16*UKT inputs, 64-input chunks
   static constexpr int kStageBytes = kWUnitBytes + kXrUnitBytes;
   static constexpr int kStagesFit = (kSmemBudget - kDbufBytes - 8192 - 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit < 12 ? kStagesFit : 12;
@@ -104,10 +105,10 @@ __device__ __forceinline__ int partial_slot(int c, int b, const MmaParams& p) {
   return b == first_block ? 0 : 1;
 }
 
-template <int BITS>
+template <int BITS, int UKT>
 struct Layout {
-  static constexpr int kStages = Cfg<BITS>::kStages;
-  static constexpr int kStageBytes = Cfg<BITS>::kStageBytes;
+  static constexpr int kStages = Cfg<BITS, UKT>::kStages;
+  static constexpr int kStageBytes = Cfg<BITS, UKT>::kStageBytes;
   static constexpr int kDbufOff = kStages * kStageBytes;        // [2][groups][16][128] fp32 sums
   static constexpr int kXchOff = kDbufOff + kDbufBytes;          // [16][128] fp32 for the rotation
   static constexpr int kBarOff = kXchOff + 8192;
@@ -131,11 +132,12 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // Either way a unit lands in shared memory as [8 k-tiles][8 tiles].
 enum { kLayoutTiles = 0, kLayoutStrips = 1 };
 
-template <int BITS, bool TWO_HALVES, int LAYOUT>
+template <int BITS, bool TWO_HALVES, int LAYOUT, int UKT>
 __global__ void __launch_bounds__(kThreads, 1)
     trellis_linear_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                               const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
-  using L = Layout<BITS>;
+  using L = Layout<BITS, UKT>;
+  using C = Cfg<BITS, UKT>;
   constexpr int S = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* dbuf = reinterpret_cast<float*>(smem + L::kDbufOff);
@@ -196,10 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_u32(smem + i * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(i), L::kStageBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(i));
+          tma_load_2d(st, &wmap, b * 32 * BITS, ub * UKT, full_bar(i));
         else
-          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * Cfg<BITS>::kWUnitBytes,
-                       Cfg<BITS>::kWUnitBytes, full_bar(i));
+          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * C::kWUnitBytes,
+                       C::kWUnitBytes, full_bar(i));
         if (++ub == UB) {
           ub = 0;
           ++b;
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pdl_wait_prerequisites();
       ub = ub_first;
       for (int i = 0; i < pre; ++i) {
-        tma_load_3d(smem_u32(smem + i * L::kStageBytes) + Cfg<BITS>::kWUnitBytes, &xmap, 0, 0, ub * 2,
+        tma_load_3d(smem_u32(smem + i * L::kStageBytes) + C::kWUnitBytes, &xmap, 0, 0, ub * (UKT / 4),
                     full_bar(i));
         if (++ub == UB) ub = 0;
       }
@@ -216,15 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       s = pre == S ? 0 : pre;
       round = pre == S ? 1 : 0;
       for (int i = pre; i < n_units; ++i) {
-        if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, abort_flag)) break;
+        if (round > 0 && !mbar_wait_sleepy(empty_bar(s), (round - 1) & 1, abort_flag, 64)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, b * 32 * BITS, ub * kUnitKt, full_bar(s));
+          tma_load_2d(st, &wmap, b * 32 * BITS, ub * UKT, full_bar(s));
         else
-          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * Cfg<BITS>::kWUnitBytes,
-                       Cfg<BITS>::kWUnitBytes, full_bar(s));
-        tma_load_3d(st + Cfg<BITS>::kWUnitBytes, &xmap, 0, 0, ub * 2, full_bar(s));
+          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * C::kWUnitBytes,
+                       C::kWUnitBytes, full_bar(s));
+        tma_load_3d(st + C::kWUnitBytes, &xmap, 0, 0, ub * (UKT / 4), full_bar(s));
         issued = i + 1;
         if (++ub == UB) {
           ub = 0;
@@ -270,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint8_t* st = smem + s * L::kStageBytes;
         const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
-        const uint8_t* xs = st + Cfg<BITS>::kWUnitBytes;
+        const uint8_t* xs = st + C::kWUnitBytes;
 #pragma unroll
-        for (int kt = 0; kt < kUnitKt; ++kt) {
+        for (int kt = 0; kt < UKT; ++kt) {
           const uint32_t* tw = wtile + kt * 64 * BITS;
           uint32_t a[4];
           decode_group4<BITS>(tw, g, t, a[0], a[2]);
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = static_cast<int>(bb);
       const int sg = static_cast<int>(bb - b_first);
       const int d = sg & 1;
-      const bool ok = mbar_wait(dfull_bar(d), (sg >> 1) & 1, abort_flag);
+      const bool ok = mbar_wait_sleepy(dfull_bar(d), (sg >> 1) & 1, abort_flag, 256);
       if (!group_all(1, 128, ok)) break;  // the group's named barriers need all 128 threads
       float v[16];
       const float* db = dbuf + d * kGroups * 2048;
@@ -393,21 +395,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BITS, bool TWO, int LAYOUT>
+template <int BITS, bool TWO, int LAYOUT, int UKT>
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, TWO, LAYOUT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS>::kBytes);
+    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, TWO, LAYOUT, UKT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS, UKT>::kBytes);
   });
   return err;
 }
 
-template <int BITS, bool TWO, int LAYOUT>
+template <int BITS, bool TWO, int LAYOUT, int UKT>
 cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
                        cudaStream_t stream) {
-  cudaError_t e = set_smem_attr<BITS, TWO, LAYOUT>();
+  cudaError_t e = set_smem_attr<BITS, TWO, LAYOUT, UKT>();
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: this kernel may start while the
   // kernel before it (the input rotation) finishes; its producer waits for
@@ -418,21 +420,25 @@ cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const M
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<BITS>::kBytes;
+  cfg.dynamicSmemBytes = Layout<BITS, UKT>::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, trellis_linear_mma_kernel<BITS, TWO, LAYOUT>, wmap, xmap, p);
+  return cudaLaunchKernelEx(&cfg, trellis_linear_mma_kernel<BITS, TWO, LAYOUT, UKT>, wmap, xmap, p);
 }
 
-template <int BITS, int LAYOUT>
+template <int BITS, int LAYOUT, int UKT>
 cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
                        cudaStream_t stream) {
-  return p.rows > 8 ? launch_one<BITS, true, LAYOUT>(wmap, xmap, p, ctas, stream)
-                    : launch_one<BITS, false, LAYOUT>(wmap, xmap, p, ctas, stream);
+  return p.rows > 8 ? launch_one<BITS, true, LAYOUT, UKT>(wmap, xmap, p, ctas, stream)
+                    : launch_one<BITS, false, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
 }
 
-template <int BITS>
+// k-tiles per unit (one rule for the CTA count and the launch): 16 where the
+// input count allows it and at least five stages still fit, else 8.
+int unit_kt(int in_features, int bits) { return (in_features % 256 == 0 && bits <= 5) ? 16 : 8; }
+
+template <int BITS, int UKT>
 cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -443,7 +449,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
                                 static_cast<cuuint64_t>(lp.in_features / 16)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.out_features) * BITS * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(kUnitKt)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(UKT)};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(lp.trellis), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -457,7 +463,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows),
                                 static_cast<cuuint64_t>(lp.in_features / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};
-    const cuuint32_t box[3] = {64, 16, 2};
+    const cuuint32_t box[3] = {64, 16, static_cast<cuuint32_t>(UKT / 4)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -471,35 +477,42 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
   p.partials = ws.partials;
   p.counters = ws.counters;
   p.err_flag = ws.err_flag;
-  p.units_per_block = lp.in_features / 128;
+  p.units_per_block = lp.in_features / (16 * UKT);
   p.units = static_cast<long long>(lp.out_features / 128) * p.units_per_block;
   p.ctas = ws.ctas;
   p.out_f32 = lp.out_f32;
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
-  return strips ? launch_mma<BITS, kLayoutStrips>(wmap, xmap, p, ws.ctas, stream)
-                : launch_mma<BITS, kLayoutTiles>(wmap, xmap, p, ws.ctas, stream);
+  return strips ? launch_mma<BITS, kLayoutStrips, UKT>(wmap, xmap, p, ws.ctas, stream)
+                : launch_mma<BITS, kLayoutTiles, UKT>(wmap, xmap, p, ws.ctas, stream);
 }
 
 }  // namespace
 
-int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features) {
-  const long long units = static_cast<long long>(out_features / 128) * (in_features / 128);
+int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features, int bits) {
+  const long long units =
+      static_cast<long long>(out_features / 128) * (in_features / (16 * unit_kt(in_features, bits)));
   return static_cast<int>(units < num_sms ? units : num_sms);
+}
+
+template <int UKT>
+cudaError_t dispatch_bits(const LinearPass& p, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
+  switch (p.bits) {
+    case 2: return run_mma<2, UKT>(p, ws, strips, stream);
+    case 3: return run_mma<3, UKT>(p, ws, strips, stream);
+    case 4: return run_mma<4, UKT>(p, ws, strips, stream);
+    case 5: return run_mma<5, UKT>(p, ws, strips, stream);
+    case 6: return run_mma<6, UKT>(p, ws, strips, stream);
+    case 8: return run_mma<8, UKT>(p, ws, strips, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
                                       cudaStream_t stream) {
-  switch (p.bits) {
-    case 2: return run_mma<2>(p, ws, strips, stream);
-    case 3: return run_mma<3>(p, ws, strips, stream);
-    case 4: return run_mma<4>(p, ws, strips, stream);
-    case 5: return run_mma<5>(p, ws, strips, stream);
-    case 6: return run_mma<6>(p, ws, strips, stream);
-    case 8: return run_mma<8>(p, ws, strips, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  return unit_kt(p.in_features, p.bits) == 16 ? dispatch_bits<16>(p, ws, strips, stream)
+                                      : dispatch_bits<8>(p, ws, strips, stream);
 }
 
 }  // namespace tfx

@@ -87,7 +87,7 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
   ws.counters = reinterpret_cast<int*>(scratch + kPartialFloats * sizeof(float));
   ws.err_flag = err_flag;
   ws.ctas = trellis_linear_mma_ctas(num_sms < kNoAllocMaxCtas ? num_sms : kNoAllocMaxCtas, in_features,
-                                   out_features);
+                                    out_features, bits);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The counters must start at zero; a completed launch leaves them at zero,
   // but clear the ones this call uses in case an earlier launch was cut short.
