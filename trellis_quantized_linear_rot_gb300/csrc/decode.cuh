@@ -195,6 +195,61 @@ struct Group4 {
   static constexpr int kWords = (3 * BITS + 16 + 31 <= 64) ? 2 : 3;
 };
 
+// Where a lane's group of four stream weights starts: word index and bit
+// offset inside it (per lane constants, computed once).
+template <int BITS>
+struct Group4Pos {
+  int w0, w1, w2, off;
+  __device__ __forceinline__ Group4Pos(int n, int t) {
+    using G = Group4<BITS>;
+    const int start = ((16 * n + 4 * t) * BITS + BITS - 16 + G::kTileBits) % G::kTileBits;
+    w0 = start >> 5;
+    off = start & 31;
+    w1 = (w0 + 1 == G::kTileWords) ? 0 : w0 + 1;
+    w2 = (w1 + 1 == G::kTileWords) ? 0 : w1 + 1;
+  }
+};
+
+// The words a group needs (loads only).
+template <int BITS>
+struct Group4Words {
+  uint32_t x[Group4<BITS>::kWords];
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_group4(const uint32_t* tw, const Group4Pos<BITS>& q, Group4Words<BITS>& gw) {
+  gw.x[0] = tw[q.w0];
+  gw.x[1] = tw[q.w1];
+  if constexpr (Group4<BITS>::kWords == 3) gw.x[2] = tw[q.w2];
+}
+
+// The arithmetic: packs weights (4t, 4t+1) and (4t+2, 4t+3) as two half2 words.
+template <int BITS>
+__device__ __forceinline__ void decode_group4_words(const Group4Words<BITS>& gw, int off, uint32_t& lo,
+                                                    uint32_t& hi) {
+  uint32_t s[4];
+  if constexpr (Group4<BITS>::kWords == 2) {
+    const uint32_t p = __funnelshift_l(gw.x[1], gw.x[0], off);  // first window at the top
+    if constexpr (BITS == 4) {
+      const uint32_t p4 = p >> 4;
+      s[0] = hi16(p);
+      s[1] = mid16(p4);
+      s[2] = mid16(p);
+      s[3] = lo16(p4);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[j] = (p >> (16 - j * BITS)) & 0xFFFFu;
+    }
+  } else {
+    const uint32_t a0 = __funnelshift_l(gw.x[1], gw.x[0], off);
+    const uint32_t a1 = __funnelshift_l(gw.x[2], gw.x[1], off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] = __funnelshift_l(a1, a0, j * BITS) >> 16;
+  }
+  lo = mul1_pair(mul1_half_plus_1024(s[0]), mul1_half_plus_1024(s[1]));
+  hi = mul1_pair(mul1_half_plus_1024(s[2]), mul1_half_plus_1024(s[3]));
+}
+
 // Packs weights (4t, 4t+1) and (4t+2, 4t+3) of output n as two half2 words.
 template <int BITS>
 __device__ __forceinline__ void decode_group4(const uint32_t* tw, int n, int t, uint32_t& lo, uint32_t& hi) {

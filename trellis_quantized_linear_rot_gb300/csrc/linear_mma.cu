@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s = pre == S ? 0 : pre;
       round = pre == S ? 1 : 0;
       for (int i = pre; i < n_units; ++i) {
-        if (round > 0 && !mbar_wait_sleepy(empty_bar(s), (round - 1) & 1, abort_flag, 64)) break;
+        if (round > 0 && !mbar_wait_sleepy(empty_bar(s), (round - 1) & 1, abort_flag, 128)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
         if (LAYOUT == kLayoutTiles)
@@ -255,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int xoff[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) xoff[q] = g * 128 + (((2 * q + (t >> 1)) ^ g) << 4) + (t & 1) * 8;
+    const Group4Pos<BITS> pos_a(g, t);      // output g of the tile
+    const Group4Pos<BITS> pos_b(g + 8, t);  // output g + 8
     bool stop = false;
     for (long long bb = b_first; bb <= b_last && !stop; ++bb) {
       const int sg = static_cast<int>(bb - b_first);
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = static_cast<int>(seg_lo) + ((cg - static_cast<int>(seg_lo)) % kGroups + kGroups) % kGroups;
       for (; i < seg_hi; i += kGroups) {
         const int s = i % S;
-        const bool ok = mbar_wait(full_bar(s), (i / S) & 1, abort_flag);
+        const bool ok = mbar_wait_sleepy(full_bar(s), (i / S) & 1, abort_flag, 32);
         if (!__all_sync(0xffffffffu, ok)) {
           stop = true;
           break;
@@ -273,19 +275,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* st = smem + s * L::kStageBytes;
         const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
         const uint8_t* xs = st + C::kWUnitBytes;
+        // Software pipeline over k-tiles: the words and B fragments of tile
+        // kt + 1 are loaded before tile kt is decoded.
+        Group4Words<BITS> wa, wb;
+        load_group4<BITS>(wtile, pos_a, wa);
+        load_group4<BITS>(wtile, pos_b, wb);
+        uint2 b_lo = *reinterpret_cast<const uint2*>(xs + xoff[0]);
+        uint2 b_hi = TWO_HALVES ? *reinterpret_cast<const uint2*>(xs + xoff[0] + 1024) : make_uint2(0u, 0u);
 #pragma unroll
         for (int kt = 0; kt < UKT; ++kt) {
-          const uint32_t* tw = wtile + kt * 64 * BITS;
+          Group4Words<BITS> na, nb;
+          uint2 nlo = make_uint2(0u, 0u), nhi = make_uint2(0u, 0u);
+          if (kt + 1 < UKT) {
+            const uint32_t* tn = wtile + (kt + 1) * 64 * BITS;
+            load_group4<BITS>(tn, pos_a, na);
+            load_group4<BITS>(tn, pos_b, nb);
+            const uint8_t* xn = xs + ((kt + 1) >> 2) * 2048 + xoff[(kt + 1) & 3];
+            nlo = *reinterpret_cast<const uint2*>(xn);
+            if (TWO_HALVES) nhi = *reinterpret_cast<const uint2*>(xn + 1024);
+          }
           uint32_t a[4];
-          decode_group4<BITS>(tw, g, t, a[0], a[2]);
-          decode_group4<BITS>(tw, g + 8, t, a[1], a[3]);
-          // xr rows g and g + 8, inputs 16kt + 4t .. +3.
-          const uint8_t* xb = xs + (kt >> 2) * 2048 + xoff[kt & 3];
-          const uint2 b_lo = *reinterpret_cast<const uint2*>(xb);
+          decode_group4_words<BITS>(wa, pos_a.off, a[0], a[2]);
+          decode_group4_words<BITS>(wb, pos_b.off, a[1], a[3]);
           mma_16816(d0, a, b_lo.x, b_lo.y);
-          if (TWO_HALVES) {
-            const uint2 b_hi = *reinterpret_cast<const uint2*>(xb + 1024);
-            mma_16816(d1, a, b_hi.x, b_hi.y);
+          if (TWO_HALVES) mma_16816(d1, a, b_hi.x, b_hi.y);
+          if (kt + 1 < UKT) {
+            wa = na;
+            wb = nb;
+            b_lo = nlo;
+            b_hi = nhi;
           }
         }
         __syncwarp();
@@ -325,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = static_cast<int>(bb);
       const int sg = static_cast<int>(bb - b_first);
       const int d = sg & 1;
-      const bool ok = mbar_wait_sleepy(dfull_bar(d), (sg >> 1) & 1, abort_flag, 256);
+      const bool ok = mbar_wait_sleepy(dfull_bar(d), (sg >> 1) & 1, abort_flag, 1000);
       if (!group_all(1, 128, ok)) break;  // the group's named barriers need all 128 threads
       float v[16];
       const float* db = dbuf + d * kGroups * 2048;
