@@ -329,7 +329,7 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_blocks = 48
+        n_blocks = 120
         secs, covered = oracle_sample(n_blocks, ROWS)
         cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "%d of 1010 output blocks (5120x128 weights each) for each of rows {1,8,16}, "
