@@ -13,6 +13,14 @@ copies alternate between calls, so no call finds its weights in L2.
 Metric: weight GB/s = packed weight bytes streamed / time, with the fraction
 of the measured HBM copy bandwidth it reaches. Prints one JSON line.
 
+Roofline: the linear is bound by the decode's integer arithmetic, not by HBM.
+Decoding one weight takes four 32-bit lane operations (cut its 16-bit window
+out of the stream, multiply by the mul1 constant, sum the product's bytes, one
+fp16 fma); an SM issues one warp instruction (32 lane operations) per cycle in
+each of its four sub-partitions, so the peak is SMs x 4 x 32 x the maximum SM
+clock. The line's "roofline" reports that bound (unit: tera lane-ops/s) and,
+under "hbm", the fraction of the measured copy bandwidth.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Multi-GPU: the path has no exchange step; N processes run N independent
@@ -49,6 +57,11 @@ def launch_bytes(rows):
     return weight_bytes() + rows * IN_F * 2 + OUT_F * 2 + rows * OUT_F * 4
 
 
+# Lane operations the method's decode needs per weight: window cut, 32-bit
+# multiply, byte sum, fp16 fma.
+DECODE_OPS_PER_WEIGHT = 4
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -56,6 +69,22 @@ def measured_peaks():
             d = json.load(fh)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def max_sm_mhz():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        if d.get("sm_max_mhz"):
+            return float(d["sm_max_mhz"])
+    return 2070.0
+
+
+def alu_peak_tops(num_sms):
+    """Issue-slot peak in tera lane-ops/s: one warp instruction per cycle in
+    each of an SM's four sub-partitions."""
+    return num_sms * 4 * 32 * max_sm_mhz() * 1e6 / 1e12
 
 
 def kernel_hash():
@@ -283,16 +312,20 @@ def run_ours(args):
 
     # Dominant kernel: the linear launches, timed by events on their stream.
     per_rows = {}
-    dur_sum, byte_sum = 0.0, 0
+    dur_sum, byte_sum, launches = 0.0, 0, 0
     for r in ROWS:
         ds = [a.elapsed_time(b) for a, b in ev[r]]
         per_rows[r] = {"us_median": statistics.median(ds) * 1e3,
                        "weight_gbs": weight_bytes() / (statistics.median(ds) * 1e-3) / 1e9}
         dur_sum += sum(ds)
         byte_sum += launch_bytes(r) * len(ds)
+        launches += len(ds)
     achieved = byte_sum / (dur_sum * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
     traffic = profiled_traffic()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = alu_peak_tops(num_sms)
+    alu_achieved = IN_F * OUT_F * DECODE_OPS_PER_WEIGHT * launches / (dur_sum * 1e-3) / 1e12
 
     # End to end through the public API from pinned host memory.
     x_host = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).pin_memory()
@@ -345,9 +378,13 @@ def run_ours(args):
                    "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "by_rows": per_rows,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                     "kernel": "trellis_linear", "kernel_hash": kernel_hash()},
+        "roofline": {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
+                     "frac": alu_achieved / alu_peak, "traffic": traffic,
+                     "ops_per_weight": DECODE_OPS_PER_WEIGHT,
+                     "peak_source": "%d SMs x 4 issue slots x 32 lanes x %.0f MHz" % (num_sms, max_sm_mhz()),
+                     "kernel": "trellis_linear", "kernel_hash": kernel_hash(),
+                     "hbm": {"achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                             "peak_source": peak_kind}},
         "clocks": clocks.summary(),
         "e2e": None if args.no_e2e else {
             "value": e2e_value, "unit": "GB/s",
