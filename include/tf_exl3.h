@@ -104,12 +104,16 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
 /*
  * tf_trellis_linear_strips -- tf_trellis_linear on the same tiles stored in
  * the "strips" order ("Checks on this head": the decode test runs on the
- * checkpoint's tile layout and on the strips layout). A strip is one block of
- * 128 outputs stored whole: for block b < out/128 and unit u < in/128, the 64
- * tiles (kt = 8u + kk, nt = 8b + nn) follow at word
- * ((b * in/128 + u) * 64 + kk * 8 + nn) * 8 * bits, each tile's 8*bits words
- * unchanged. Each 128-input unit of a block is then one contiguous run,
- * which the GPU streams at a higher rate than the k-tile-major order.
+ * checkpoint's tile layout and on the strips layout; the page does not spell
+ * that order out, so this one is the library's own). A strip is one block of
+ * 128 outputs stored whole. Inside block b < out/128, groups of four k-tiles
+ * c < in/64 follow in input order; group c holds the 8 tiles
+ * (kt = 4c + kk, nt = 8b + nn) with their words interleaved: word w of tile
+ * (4c + kk, 8b + nn) is strips word
+ *   (((b * in/64 + c) * 8 + nn) * 8*bits + w) * 4 + kk,   kk < 4, nn < 8.
+ * Each unit of work of a block is then one contiguous run, and one 128-bit
+ * load brings a word of four k-tiles, which makes the decode cheaper than on
+ * the k-tile-major order.
  * Same arguments, results (bit for bit) and refusals as tf_trellis_linear.
  */
 tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const void* svh,

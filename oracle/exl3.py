@@ -293,21 +293,24 @@ def decode_rows(trellis, in_features, out_features, bits, ks):
 # ---------------------------------------------------------------------------
 # The second storage order of the same tiles ("Checks on this head": the
 # decode test runs on the checkpoint's tile layout and on the strips layout).
-# Reading: a strip is one block of 128 outputs; it is stored whole, unit by
-# unit (128 inputs = 8 k-tiles), each unit's 64 tiles in [k-tile][n-tile]
-# order. The tiles themselves (their 8*bits words) are unchanged.
+# Reading (the page does not specify it): a strip is one block of 128
+# outputs, stored whole; inside it, groups of four k-tiles follow in input
+# order, and a group stores its 8 n-tiles one after another with the words of
+# its four k-tiles interleaved: word w of k-tiles 4c, 4c+1, 4c+2, 4c+3 are
+# four consecutive words. Every word of the tiles appears once.
 # ---------------------------------------------------------------------------
 def tiles_to_strips(trellis, in_features, out_features, bits):
     """k-tile-major packed tiles -> strips order (same words, other order)."""
     check_shape(in_features, out_features, bits)
     kt, nt = in_features // 16, out_features // 16
-    t = np.asarray(trellis, dtype=np.uint32).reshape(kt // 8, 8, nt // 8, 8, 8 * bits)
-    # [unit][kt%8][strip][nt%8][words] -> [strip][unit][kt%8][nt%8][words]
-    return np.ascontiguousarray(t.transpose(2, 0, 1, 3, 4)).reshape(-1)
+    t = np.asarray(trellis, dtype=np.uint32).reshape(kt // 4, 4, nt // 8, 8, 8 * bits)
+    # [group][kt%4][block][nt%8][word] -> [block][group][nt%8][word][kt%4]
+    return np.ascontiguousarray(t.transpose(2, 0, 3, 4, 1)).reshape(-1)
 
 
 def strips_to_tiles(strips, in_features, out_features, bits):
     check_shape(in_features, out_features, bits)
     kt, nt = in_features // 16, out_features // 16
-    s = np.asarray(strips, dtype=np.uint32).reshape(nt // 8, kt // 8, 8, 8, 8 * bits)
-    return np.ascontiguousarray(s.transpose(1, 2, 0, 3, 4)).reshape(-1)
+    s = np.asarray(strips, dtype=np.uint32).reshape(nt // 8, kt // 4, 8, 8 * bits, 4)
+    # [block][group][nt%8][word][kt%4] -> [group][kt%4][block][nt%8][word]
+    return np.ascontiguousarray(s.transpose(1, 4, 0, 2, 3)).reshape(-1)

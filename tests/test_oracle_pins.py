@@ -472,16 +472,23 @@ def test_decode_rows_and_blocks_agree_with_matrix():
     assert np.array_equal(bits16(o.decode_blocks(tr, 256, 256, k, [1])), bits16(w[:, 128:]))
 
 
-def test_strips_layout_places_each_tile_by_hand_formula():
-    k, i_f, o_f = 2, 256, 384
+def test_strips_layout_places_each_word_by_hand_formula():
+    """Word w of tile (kt, nt) lands at word
+    (((b * I/64 + c) * 8 + nt % 8) * 8*bits + w) * 4 + kt % 4 of the strips
+    order, with b = nt // 8 and c = kt // 4."""
+    k, i_f, o_f = 3, 256, 384
     tr = synth.make_trellis(i_f, o_f, k, 91)
     st = o.tiles_to_strips(tr, i_f, o_f, k)
     per = 8 * k
-    ub = i_f // 128
+    groups = i_f // 64
+    seen = np.zeros(st.size, dtype=bool)
     for kt in range(i_f // 16):
         for nt in range(o_f // 16):
-            src = (kt * (o_f // 16) + nt) * per
-            b, u = nt // 8, kt // 8
-            dst = ((b * ub + u) * 64 + (kt % 8) * 8 + nt % 8) * per
-            assert np.array_equal(st[dst:dst + per], tr[src:src + per])
+            b, c = nt // 8, kt // 4
+            for w in range(per):
+                src = (kt * (o_f // 16) + nt) * per + w
+                dst = (((b * groups + c) * 8 + nt % 8) * per + w) * 4 + kt % 4
+                assert st[dst] == tr[src]
+                seen[dst] = True
+    assert seen.all()
     assert np.array_equal(o.strips_to_tiles(st, i_f, o_f, k), tr)

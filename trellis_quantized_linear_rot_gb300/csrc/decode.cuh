@@ -223,6 +223,38 @@ __device__ __forceinline__ void load_group4(const uint32_t* tw, const Group4Pos<
   if constexpr (Group4<BITS>::kWords == 3) gw.x[2] = tw[q.w2];
 }
 
+// Interleaved form (the strips order): the words of four consecutive k-tiles
+// are stored together, word w of k-tiles 4c .. 4c+3 forming one 16-byte
+// chunk, so one 128-bit load brings a word for four k-tiles.
+template <int BITS>
+struct Group4Quads {
+  uint4 q[Group4<BITS>::kWords];
+};
+
+// `tq` points at the tile's chunks for one group of four k-tiles.
+template <int BITS>
+__device__ __forceinline__ void load_group4_quads(const uint4* tq, const Group4Pos<BITS>& p,
+                                                  Group4Quads<BITS>& gq) {
+  gq.q[0] = tq[p.w0];
+  gq.q[1] = tq[p.w1];
+  if constexpr (Group4<BITS>::kWords == 3) gq.q[2] = tq[p.w2];
+}
+
+template <int KK>
+__device__ __forceinline__ uint32_t quad_word(const uint4& v) {
+  if constexpr (KK == 0) return v.x;
+  if constexpr (KK == 1) return v.y;
+  if constexpr (KK == 2) return v.z;
+  return v.w;
+}
+
+// The words of k-tile KK (0..3) of the group.
+template <int BITS, int KK>
+__device__ __forceinline__ void quads_to_words(const Group4Quads<BITS>& gq, Group4Words<BITS>& gw) {
+#pragma unroll
+  for (int i = 0; i < Group4<BITS>::kWords; ++i) gw.x[i] = quad_word<KK>(gq.q[i]);
+}
+
 // The arithmetic: packs weights (4t, 4t+1) and (4t+2, 4t+3) as two half2 words.
 template <int BITS>
 __device__ __forceinline__ void decode_group4_words(const Group4Words<BITS>& gw, int off, uint32_t& lo,

@@ -105,6 +105,60 @@ __device__ __forceinline__ int partial_slot(int c, int b, const MmaParams& p) {
   return b == first_block ? 0 : 1;
 }
 
+// The order in which a CTA works through its segments (one per output block
+// its range touches). When the range ends inside a block, that block is
+// shared with the next CTA, which takes its own part of it first; this CTA
+// then also takes that segment first, so both parts of every shared block
+// are summed early and no cross-CTA sum is left for the end of the kernel.
+// The order changes no result: a block's sum does not depend on when its
+// segments run. Units are indexed from the range start; a segment's units
+// are consecutive in the processing order, starting at pos().
+struct SegmentOrder {
+  long long u0, b_first, b_last;
+  int UB, n_units, n_seg, n_last;
+  bool rotated;
+  __device__ SegmentOrder(long long u0_, long long u1_, int UB_) {
+    u0 = u0_;
+    UB = UB_;
+    n_units = static_cast<int>(u1_ - u0_);
+    b_first = u0_ / UB_;
+    b_last = (u1_ - 1) / UB_;
+    n_seg = static_cast<int>(b_last - b_first) + 1;
+    n_last = n_units - lo(b_last);
+    rotated = n_seg >= 2 && (u1_ % UB_) != 0;
+  }
+  __device__ long long block(int q) const {
+    return rotated ? (q == 0 ? b_last : b_first + q - 1) : b_first + q;
+  }
+  __device__ int lo(long long bb) const { return bb * UB > u0 ? static_cast<int>(bb * UB - u0) : 0; }
+  __device__ int hi(long long bb) const {
+    const long long h = (bb + 1) * UB - u0;
+    return h < n_units ? static_cast<int>(h) : n_units;
+  }
+  // Processing position of the first unit of segment q (whose first unit is lo).
+  __device__ int pos(int q, int seg_lo) const { return rotated ? (q == 0 ? 0 : n_last + seg_lo) : seg_lo; }
+};
+
+// Walks the units of a CTA in processing order: block and unit within it.
+struct UnitCursor {
+  SegmentOrder o;
+  int q, i, end;
+  long long bb;
+  __device__ explicit UnitCursor(const SegmentOrder& order) : o(order), q(0) {
+    bb = o.block(0);
+    i = o.lo(bb);
+    end = o.hi(bb);
+  }
+  __device__ int ub() const { return static_cast<int>(o.u0 + i - bb * o.UB); }
+  __device__ void next() {
+    if (++i == end && ++q < o.n_seg) {
+      bb = o.block(q);
+      i = o.lo(bb);
+      end = o.hi(bb);
+    }
+  }
+};
+
 template <int BITS, int UKT>
 struct Layout {
   static constexpr int kStages = Cfg<BITS, UKT>::kStages;
@@ -127,9 +181,67 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// One k-tile of a compute warp: decode the lane's two runs of four weights
+// into the A fragment, then one MMA per 8 row slots.
+template <int BITS, bool TWO_HALVES>
+__device__ __forceinline__ void tile_step(const Group4Words<BITS>& wa, const Group4Words<BITS>& wb,
+                                          const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
+                                          uint2 b_lo, uint2 b_hi, float (&d0)[4], float (&d1)[4]) {
+  uint32_t a[4];
+  decode_group4_words<BITS>(wa, pos_a.off, a[0], a[2]);
+  decode_group4_words<BITS>(wb, pos_b.off, a[1], a[3]);
+  mma_16816(d0, a, b_lo.x, b_lo.y);
+  if (TWO_HALVES) mma_16816(d1, a, b_hi.x, b_hi.y);
+}
+
+template <int BITS, bool TWO_HALVES, int KK>
+__device__ __forceinline__ void quad_step(const Group4Quads<BITS>& qa, const Group4Quads<BITS>& qb,
+                                          const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
+                                          const uint8_t* xg, const int (&xoff)[4], float (&d0)[4],
+                                          float (&d1)[4]) {
+  Group4Words<BITS> wa, wb;
+  quads_to_words<BITS, KK>(qa, wa);
+  quads_to_words<BITS, KK>(qb, wb);
+  const uint2 b_lo = *reinterpret_cast<const uint2*>(xg + xoff[KK]);
+  const uint2 b_hi = TWO_HALVES ? *reinterpret_cast<const uint2*>(xg + xoff[KK] + 1024) : make_uint2(0u, 0u);
+  tile_step<BITS, TWO_HALVES>(wa, wb, pos_a, pos_b, b_lo, b_hi, d0, d1);
+}
+
+// A unit in the strips order: `tq` is the warp's tile in the first group of
+// four k-tiles (chunk (c, tile, word) at (c * 8 + tile) * 8 * bits + word);
+// one 128-bit load per word brings it for four k-tiles, and the next group's
+// chunks are loaded while the current group is decoded.
+template <int BITS, bool TWO_HALVES, int UKT>
+__device__ __forceinline__ void strips_unit(const uint4* tq, const uint8_t* xs, const int (&xoff)[4],
+                                            const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
+                                            float (&d0)[4], float (&d1)[4]) {
+  Group4Quads<BITS> qa, qb;
+  load_group4_quads<BITS>(tq, pos_a, qa);
+  load_group4_quads<BITS>(tq, pos_b, qb);
+#pragma unroll
+  for (int c = 0; c < UKT / 4; ++c) {
+    Group4Quads<BITS> na, nb;
+    if (c + 1 < UKT / 4) {
+      load_group4_quads<BITS>(tq + (c + 1) * 64 * BITS, pos_a, na);
+      load_group4_quads<BITS>(tq + (c + 1) * 64 * BITS, pos_b, nb);
+    }
+    const uint8_t* xg = xs + c * 2048;
+    quad_step<BITS, TWO_HALVES, 0>(qa, qb, pos_a, pos_b, xg, xoff, d0, d1);
+    quad_step<BITS, TWO_HALVES, 1>(qa, qb, pos_a, pos_b, xg, xoff, d0, d1);
+    quad_step<BITS, TWO_HALVES, 2>(qa, qb, pos_a, pos_b, xg, xoff, d0, d1);
+    quad_step<BITS, TWO_HALVES, 3>(qa, qb, pos_a, pos_b, xg, xoff, d0, d1);
+    if (c + 1 < UKT / 4) {
+      qa = na;
+      qb = nb;
+    }
+  }
+}
+
 // Weight layouts: k-tile major ("tiles": tile (kt, nt) at (kt*O/16 + nt)),
-// or block-contiguous ("strips": block b, unit u, then [kt % 8][nt % 8]).
-// Either way a unit lands in shared memory as [8 k-tiles][8 tiles].
+// landing in shared memory as [k-tile][8 tiles][words]; or block-contiguous
+// with the words of four consecutive k-tiles interleaved ("strips": block b,
+// then groups of four k-tiles, then [tile % 8][word][k-tile % 4]), landing as
+// [k-tile / 4][8 tiles][words][k-tile % 4].
 enum { kLayoutTiles = 0, kLayoutStrips = 1 };
 
 template <int BITS, bool TWO_HALVES, int LAYOUT, int UKT>
@@ -156,13 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   constexpr int kProducerWarp = 4 + kComputeWarps;
   const int c = blockIdx.x;
-  const long long u0 = range_start(c, p.units, p.ctas);
-  const long long u1 = range_start(c + 1, p.units, p.ctas);
-  const int n_units = static_cast<int>(u1 - u0);
-  const int UB = p.units_per_block;
-  const long long b_first = u0 / UB;
-  const long long b_last = (u1 - 1) / UB;
-  const int ub_first = static_cast<int>(u0 - b_first * UB);
+  const SegmentOrder order(range_start(c, p.units, p.ctas), range_start(c + 1, p.units, p.ctas),
+                           p.units_per_block);
+  const int n_units = order.n_units;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -187,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
-      int b = static_cast<int>(b_first);
-      int ub = ub_first;
+      UnitCursor cur(order);
+      UnitCursor xcur(order);
       int s = 0;
       int round = 0;
       // The first stages' weight copies need nothing from the kernel before
@@ -198,21 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_u32(smem + i * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(i), L::kStageBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, b * 32 * BITS, ub * UKT, full_bar(i));
+          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(i));
         else
-          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * C::kWUnitBytes,
-                       C::kWUnitBytes, full_bar(i));
-        if (++ub == UB) {
-          ub = 0;
-          ++b;
-        }
+          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * C::kWUnitBytes, C::kWUnitBytes,
+                       full_bar(i));
+        cur.next();
       }
       pdl_wait_prerequisites();
-      ub = ub_first;
       for (int i = 0; i < pre; ++i) {
-        tma_load_3d(smem_u32(smem + i * L::kStageBytes) + C::kWUnitBytes, &xmap, 0, 0, ub * (UKT / 4),
+        tma_load_3d(smem_u32(smem + i * L::kStageBytes) + C::kWUnitBytes, &xmap, 0, 0, xcur.ub() * (UKT / 4),
                     full_bar(i));
-        if (++ub == UB) ub = 0;
+        xcur.next();
       }
       issued = pre;
       s = pre == S ? 0 : pre;
@@ -222,16 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, b * 32 * BITS, ub * UKT, full_bar(s));
+          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(s));
         else
-          bulk_load_1d(st, p.strips + (static_cast<size_t>(b) * UB + ub) * C::kWUnitBytes,
-                       C::kWUnitBytes, full_bar(s));
-        tma_load_3d(st + C::kWUnitBytes, &xmap, 0, 0, ub * (UKT / 4), full_bar(s));
+          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * C::kWUnitBytes, C::kWUnitBytes,
+                       full_bar(s));
+        tma_load_3d(st + C::kWUnitBytes, &xmap, 0, 0, cur.ub() * (UKT / 4), full_bar(s));
         issued = i + 1;
-        if (++ub == UB) {
-          ub = 0;
-          ++b;
-        }
+        cur.next();
         if (++s == S) {
           s = 0;
           ++round;
@@ -258,23 +359,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Group4Pos<BITS> pos_a(g, t);      // output g of the tile
     const Group4Pos<BITS> pos_b(g + 8, t);  // output g + 8
     bool stop = false;
-    for (long long bb = b_first; bb <= b_last && !stop; ++bb) {
-      const int sg = static_cast<int>(bb - b_first);
-      const long long seg_lo = bb * UB > u0 ? bb * UB - u0 : 0;
-      const long long seg_hi = (bb + 1) * UB - u0 < n_units ? (bb + 1) * UB - u0 : n_units;
+    for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
+      const long long bb = order.block(sg);
+      const int seg_lo = order.lo(bb);
+      const int seg_hi = order.hi(bb);
+      const int base = order.pos(sg, seg_lo) - seg_lo;  // processing position of unit i: base + i
       float d0[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 0..7
       float d1[4] = {0.f, 0.f, 0.f, 0.f};  // row slots 8..15
-      int i = static_cast<int>(seg_lo) + ((cg - static_cast<int>(seg_lo)) % kGroups + kGroups) % kGroups;
+      int i = seg_lo + ((cg - seg_lo) % kGroups + kGroups) % kGroups;
       for (; i < seg_hi; i += kGroups) {
-        const int s = i % S;
-        const bool ok = mbar_wait_sleepy(full_bar(s), (i / S) & 1, abort_flag, 32);
+        const int k = base + i;
+        const int s = k % S;
+        const bool ok = mbar_wait_sleepy(full_bar(s), (k / S) & 1, abort_flag, 32);
         if (!__all_sync(0xffffffffu, ok)) {
           stop = true;
           break;
         }
         const uint8_t* st = smem + s * L::kStageBytes;
-        const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
         const uint8_t* xs = st + C::kWUnitBytes;
+        if constexpr (LAYOUT == kLayoutStrips) {
+          strips_unit<BITS, TWO_HALVES, UKT>(reinterpret_cast<const uint4*>(st) + j * 8 * BITS, xs, xoff, pos_a,
+                                              pos_b, d0, d1);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(s));
+          continue;
+        }
+        const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
         // Software pipeline over k-tiles: the words and B fragments of tile
         // kt + 1 are loaded before tile kt is decoded.
         Group4Words<BITS> wa, wb;
@@ -339,9 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     lp.rows = p.rows;
     lp.in_features = p.in_features;
     lp.out_features = p.out_features;
-    for (long long bb = b_first; bb <= b_last; ++bb) {
-      const int b = static_cast<int>(bb);
-      const int sg = static_cast<int>(bb - b_first);
+    for (int sg = 0; sg < order.n_seg; ++sg) {
+      const int b = static_cast<int>(order.block(sg));
       const int d = sg & 1;
       const bool ok = mbar_wait_sleepy(dfull_bar(d), (sg >> 1) & 1, abort_flag, 1000);
       if (!group_all(1, 128, ok)) break;  // the group's named barriers need all 128 threads
@@ -355,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 16; ++r) v[r] = __fadd_rn(v[r], db[q * 2048 + r * 128 + t]);
       __syncwarp();
       if (lane == 0) mbar_arrive(dempty_bar(d));
-      const int c_first = cta_of_unit(static_cast<long long>(b) * UB, p.units, p.ctas);
-      const int c_last = cta_of_unit(static_cast<long long>(b + 1) * UB - 1, p.units, p.ctas);
+      const int c_first = cta_of_unit(static_cast<long long>(b) * order.UB, p.units, p.ctas);
+      const int c_last = cta_of_unit(static_cast<long long>(b + 1) * order.UB - 1, p.units, p.ctas);
       if (c_first == c_last) {
         block_epilogue(v, lp, b, t, xch, 1, 128);
         continue;
@@ -379,13 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = c_first; cc <= c_last; ++cc) {
           const float* src =
               p.partials + (static_cast<size_t>(cc) * 2 + partial_slot(cc, b, p)) * 16 * 128;
+          // All 16 row slots are loaded at once (slots past `rows` hold stale
+          // values that are never used), so the loads overlap.
+          float x[16];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) {
-            if (r < p.rows) {
-              const float x = __ldcg(src + r * 128 + t);
-              v[r] = (cc == c_first) ? x : __fadd_rn(v[r], x);
-            }
-          }
+          for (int r = 0; r < 16; ++r) x[r] = __ldcg(src + r * 128 + t);
+#pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (r < p.rows) v[r] = (cc == c_first) ? x[r] : __fadd_rn(v[r], x[r]);
         }
         block_epilogue(v, lp, b, t, xch, 1, 128);
         if (t == 0) p.counters[b] = 0;

@@ -35,25 +35,31 @@ __global__ void __launch_bounds__(128) trellis_decode_kernel(const uint32_t* __r
   }
 }
 
-// Tiles -> strips: one 16-byte chunk per thread, written in strips order.
-// Strips order: block b of 128 outputs, then unit u of 128 inputs, then
-// [k-tile % 8][n-tile % 8], each tile's 8*bits words unchanged.
-__global__ void __launch_bounds__(256) tiles_to_strips_kernel(const uint4* __restrict__ tiles,
+// Tiles -> strips: one 16-byte chunk of the strips order per thread.
+// Strips order: block b of 128 outputs, then group c of four k-tiles, then
+// [n-tile % 8][word w][k-tile % 4]; chunk (b, c, nn, w) holds word w of the
+// tiles (4c + kk, 8b + nn), kk = 0..3. The four words come from four k-tile
+// rows of the tiles order; consecutive threads read consecutive words of one
+// tile, so each of the four loads is coalesced.
+__global__ void __launch_bounds__(256) tiles_to_strips_kernel(const uint32_t* __restrict__ tiles,
                                                               uint4* __restrict__ strips,
-                                                              long long chunks, int chunks_per_tile,
-                                                              int units_per_block, int n_tiles) {
+                                                              long long chunks, int tile_words,
+                                                              int groups_per_block, int n_tiles) {
+  const long long row_words = static_cast<long long>(n_tiles) * tile_words;  // one k-tile row
   for (long long q = blockIdx.x * 256LL + threadIdx.x; q < chunks; q += static_cast<long long>(gridDim.x) * 256) {
-    const long long td = q / chunks_per_tile;
-    const int within = static_cast<int>(q - td * chunks_per_tile);
-    const long long per_block = static_cast<long long>(units_per_block) * 64;
-    const long long b = td / per_block;
-    const int rem = static_cast<int>(td - b * per_block);
-    const int u = rem >> 6;
-    const int kk = (rem >> 3) & 7;
-    const int nn = rem & 7;
-    const long long kt = 8LL * u + kk;
-    const long long nt = 8LL * b + nn;
-    strips[q] = tiles[(kt * n_tiles + nt) * chunks_per_tile + within];
+    const long long tq = q / tile_words;  // (b, c, nn)
+    const int w = static_cast<int>(q - tq * tile_words);
+    const int nn = static_cast<int>(tq & 7);
+    const long long bc = tq >> 3;         // b * groups_per_block + c
+    const long long b = bc / groups_per_block;
+    const long long c = bc - b * groups_per_block;
+    const uint32_t* src = tiles + (4 * c * n_tiles + 8 * b + nn) * tile_words + w;
+    uint4 v;
+    v.x = src[0];
+    v.y = src[row_words];
+    v.z = src[2 * row_words];
+    v.w = src[3 * row_words];
+    strips[q] = v;
   }
 }
 
@@ -84,13 +90,13 @@ struct DecodeLauncher {
 
 cudaError_t launch_tiles_to_strips(const uint32_t* tiles, uint32_t* strips, int in_features,
                                    int out_features, int bits, cudaStream_t stream) {
-  const int chunks_per_tile = 2 * bits;  // 8 * bits words = 2 * bits chunks of 16 bytes
-  const long long chunks = static_cast<long long>(in_features / 16) * (out_features / 16) * chunks_per_tile;
+  const int tile_words = 8 * bits;
+  // One chunk per (block, group of four k-tiles, tile, word).
+  const long long chunks = static_cast<long long>(in_features / 64) * (out_features / 16) * tile_words;
   long long grid = (chunks + 255) / 256;
   if (grid > 152LL * 16) grid = 152LL * 16;
   tiles_to_strips_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(tiles), reinterpret_cast<uint4*>(strips), chunks, chunks_per_tile,
-      in_features / 128, out_features / 16);
+      tiles, reinterpret_cast<uint4*>(strips), chunks, tile_words, in_features / 64, out_features / 16);
   return cudaGetLastError();
 }
 
