@@ -78,9 +78,12 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
  *             the packed trellis (format below), never written to memory
  *   acc[r][n] = sum_k xr[r][k] * W[k][n]      (fp16 products, fp32 sums in a
  *             fixed order: a row's bits do not depend on the other rows)
- *   y[r][n] = fp32_or_fp16( FWHT128(acc[r][block of n])[n] * fp32(1/sqrt(128))
- *                           * fp32(svh[n]) )   (two fp32 multiplies, then one
- *             rounding when out_dtype is TF_F16; overflow gives +-inf)
+ *   y[r][n] = out( FWHT128(acc[r][block of n])[n] * fp32(1/sqrt(128))
+ *                  * fp32(svh[n]) )   (two fp32 multiplies; out() stores the
+ *             fp32 value for TF_F32, or rounds it once, to nearest with ties
+ *             to even, to fp16 (TF_F16) or bf16 (TF_BF16; "Checks on this
+ *             head": the linear at 4 bits with bf16 out); overflow gives
+ *             +-inf)
  * xr:      [rows][in_features] fp16 (the output of tf_rot_in)
  * trellis: packed tiles, tf_trellis_bytes(in, out, bits) bytes:
  *   tile (kt, nt), kt < in/16, nt < out/16, is 8*bits uint32 words starting
@@ -92,7 +95,7 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
  *   mod 2^32, s = sum of u's four bytes, weight = fp16 fma s * 0x1EEE + 0xC2E8
  *   (fp16 bit patterns; 0x1EEE = 0.00676727294921875, 0xC2E8 = -3.453125).
  * svh:     [out_features] fp16
- * y:       [rows][out_features], out_dtype TF_F16 or TF_F32, written
+ * y:       [rows][out_features], out_dtype TF_F16, TF_F32 or TF_BF16, written
  * rows >= 0 (0 launches nothing; more than 16 runs passes of 16 rows, each
  * re-reading the weights); in/out_features positive multiples of 128;
  * bits in {2, 3, 4, 5, 6, 8}. All pointers 16-byte aligned.

@@ -271,6 +271,23 @@ def epilogue_f32(acc32, svh):
     return y * np.asarray(svh).astype(np.float32)
 
 
+def bf16_bits_rne(y32):
+    """float32 values -> bf16 bit patterns (uint16), rounded once to nearest
+    with ties to even ("Checks on this head": the linear at 4 bits with bf16
+    out). bf16 keeps the top 16 bits of the float32 pattern; the dropped low
+    16 bits round the kept part up when they exceed half of its last place,
+    or equal half and the kept last bit is odd. A carry out of the fraction
+    moves to the next exponent, so the largest values round to infinity.
+    NaN stays NaN (quiet, sign kept)."""
+    y = np.asarray(y32, dtype=np.float32)
+    b = y.view(np.uint32).astype(np.uint64)
+    kept, dropped = b >> 16, b & 0xFFFF
+    up = (dropped > 0x8000) | ((dropped == 0x8000) & ((kept & 1) == 1))
+    out = kept + up.astype(np.uint64)
+    out = np.where(np.isnan(y), kept | 0x40, out)
+    return out.astype(np.uint16)
+
+
 def project_f64(x, suh, trellis, svh, in_features, out_features, bits, x_dtype="f16"):
     """The whole path: rot_in (fp32 steps, fp16 out), decode, float64 linear."""
     xr = rot_in_f32(x, suh, x_dtype)

@@ -62,3 +62,24 @@ def assert_close_f16(y16, y_ref, tol=REL_TOL):
     good = (err <= slack + half_ulp) | ok_inf
     assert np.all(good), "fp16 output outside bound at %s" % (np.argwhere(~good)[:5].tolist(),)
     return float(np.max(np.where(np.isfinite(err), err / np.maximum(rms, 1e-300), 0.0)))
+
+
+def bf16_to_f64(bits):
+    """bf16 bit patterns (uint16) -> float64 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def assert_close_bf16(ybits, y_ref, tol=REL_TOL):
+    """bf16 outputs (uint16 bit patterns): the fp32 value may be off by
+    tol * rms(row); one rounding to bf16 (8 significant bits) then adds at most
+    half a bf16 place of the value, i.e. 2^(e - 9) for a value in
+    [2^(e-1), 2^e)."""
+    y = bf16_to_f64(ybits)
+    rms = np.sqrt(np.mean(np.square(y_ref), axis=1))[:, None]
+    slack = tol * rms
+    hi = np.abs(y_ref) + slack
+    half_place = np.ldexp(1.0, np.frexp(hi)[1] - 9)
+    err = np.abs(y - y_ref)
+    good = err <= slack + half_place
+    assert np.all(good), "bf16 output outside bound at %s" % (np.argwhere(~good)[:5].tolist(),)
+    return float(np.max(err / rms))

@@ -72,7 +72,10 @@ def test_linear_refusals(lib):
     assert lin(lib, i=-128) == tf.TF_ERR_SHAPE
     assert lin(lib, bits=7) == tf.TF_ERR_BITS
     assert lin(lib, bits=1) == tf.TF_ERR_BITS
-    assert lin(lib, dt=tf.TF_BF16) == tf.TF_ERR_DTYPE
+    # bf16 output is accepted (the refusal then comes from the NULL buffer);
+    # any other code is not.
+    assert lin(lib, dt=tf.TF_BF16, xr=NUL) == tf.TF_ERR_NULL
+    assert lin(lib, dt=3) == tf.TF_ERR_DTYPE
     assert lin(lib, dt=9) == tf.TF_ERR_DTYPE
     assert lin(lib, xr=NUL) == tf.TF_ERR_NULL
     assert lin(lib, tr=NUL) == tf.TF_ERR_NULL

@@ -15,7 +15,7 @@ import pytest
 
 from oracle import exl3 as o
 from trellis_quantized_linear_rot_gb300 import synth
-from helpers import assert_close_f16, assert_close_f32, bits16, dev, dev_bf16, host
+from helpers import assert_close_bf16, assert_close_f16, assert_close_f32, bits16, dev, dev_bf16, host
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -163,6 +163,36 @@ def test_config_sweep_identity_rows_bit_exact(bits):
     assert np.array_equal(y32.view(np.uint32), want32.view(np.uint32))
     y16 = run_linear(xr, tr, svh, bits, o_f, torch.float16)
     assert np.array_equal(bits16(y16), bits16(want32.astype(np.float16)))
+    ybf = run_linear(xr, tr, svh, bits, o_f, torch.bfloat16)
+    assert np.array_equal(ybf, o.bf16_bits_rne(want32))
+
+
+@pytest.mark.parametrize("bits,rows", [(4, 1), (4, 16), (2, 5), (8, 17), (6, 3)])
+def test_linear_bf16_output(bits, rows):
+    """bf16 output: within the bound of the float64 reference, and bit for
+    bit the oracle's rounding of the same launch shape's fp32 output."""
+    i_f, o_f = 384, 512
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=20 + rows)
+    xr = o.rot_in_f32(x, suh)
+    ref = o.linear_f64(xr, o.decode_matrix(tr, i_f, o_f, bits), svh)
+    y32 = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    ybf = run_linear(xr, tr, svh, bits, o_f, torch.bfloat16)
+    assert ybf.dtype == np.uint16
+    assert np.array_equal(ybf, o.bf16_bits_rne(y32))
+    assert_close_bf16(ybf, ref)
+
+
+def test_config_head_bf16_sampled():
+    """LM head 5120 -> 129,280 at 4 bits with bf16 out (the page's bf16-output
+    registration of the linear), 1 row: sampled blocks."""
+    i_f, o_f, bits = 5120, 129280, 4
+    x, suh, svh, tr = inputs(1, i_f, o_f, bits, c=2)
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    y = host(tf.tf_trellis_linear(xr_t, dev(tr), dev(svh), bits, o_f, out_dtype=torch.bfloat16))
+    blocks = [0, 640, 1009]
+    w = o.decode_blocks(tr, i_f, o_f, bits, blocks)
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    assert_close_bf16(y[:, cols], o.linear_f64(host(xr_t), w, svh[cols]))
 
 
 @pytest.mark.parametrize("bits", o.BITS_ALLOWED)
@@ -193,6 +223,9 @@ def test_gate4_exact_sums():
     y16 = run_linear(xr, tr, svh, bits, o_f, torch.float16).astype(np.float64)
     for b in range(o_f // 128):
         assert np.isinf(y16[0, 128 * b]) and np.sign(y16[0, 128 * b]) == -np.sign(float(svh[128 * b]))
+    # bf16 has fp32's range: no overflow, one rounding of the exact fp32 values.
+    ybf = run_linear(xr, tr, svh, bits, o_f, torch.bfloat16)
+    assert np.array_equal(ybf, o.bf16_bits_rne(want))
 
 
 def test_non_finite_classes_match_float64():

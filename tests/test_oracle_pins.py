@@ -492,3 +492,34 @@ def test_strips_layout_places_each_word_by_hand_formula():
                 seen[dst] = True
     assert seen.all()
     assert np.array_equal(o.strips_to_tiles(st, i_f, o_f, k), tr)
+
+
+# ------------------------------------------------------------ bf16 output
+def test_bf16_rounding_hand_values():
+    """bf16 keeps 8 significant bits: at 1.0 the last place is 2^-7."""
+    f = lambda v: int(o.bf16_bits_rne(np.float32(v)))
+    assert f(1.0) == 0x3F80
+    assert f(1.0 + 2.0 ** -8) == 0x3F80           # half a place, kept bit even: stays
+    assert f(1.0 + 3 * 2.0 ** -8) == 0x3F82       # half a place, kept bit odd: up to even
+    assert f(1.0 + 2.0 ** -8 + 2.0 ** -20) == 0x3F81  # just above half: up
+    assert f(-2.5) == 0xC020
+    assert f(0.0) == 0x0000 and f(-0.0) == 0x8000
+    assert f(np.inf) == 0x7F80 and f(-np.inf) == 0xFF80
+    assert f(np.float32(3.4028235e38)) == 0x7F80  # the largest float32 rounds up to infinity
+    assert f(np.float32(1e-40)) == int(np.float32(1e-40).view(np.uint32)) >> 16  # subnormal, exact cut
+    n = int(o.bf16_bits_rne(np.float32(np.nan)))
+    assert (n & 0x7F80) == 0x7F80 and (n & 0x7F) != 0
+
+
+def test_bf16_rounding_matches_torch():
+    """Against torch's float32 -> bfloat16 conversion (nearest, ties to even)
+    on random patterns, exact ties and values next to them."""
+    torch = pytest.importorskip("torch")
+    g = np.random.Generator(np.random.PCG64(1234))
+    pat = g.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    ties = (g.integers(0, 2 ** 16, size=20000, dtype=np.uint64).astype(np.uint32) << 16) | 0x8000
+    pat = np.concatenate([pat, ties, ties + 1, ties - 1])
+    v = pat.view(np.float32)
+    v = v[~np.isnan(v)]
+    want = torch.from_numpy(v.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o.bf16_bits_rne(v), want)

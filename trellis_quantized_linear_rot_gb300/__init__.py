@@ -133,7 +133,8 @@ def tf_trellis_linear(xr, trellis, svh, bits, out_features, out_dtype=None, y=No
     """y = trellis linear of the rotated rows xr (see tf_trellis_linear).
 
     xr: [rows, in] fp16; trellis: packed uint32 words (torch.int32 storage);
-    svh: [out] fp16; out_dtype torch.float16 or torch.float32. Returns y.
+    svh: [out] fp16; out_dtype torch.float16, torch.float32 or torch.bfloat16.
+    Returns y.
     """
     import torch
     rows, in_f = xr.shape

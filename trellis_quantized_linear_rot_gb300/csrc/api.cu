@@ -197,7 +197,7 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
       !valid_features(out_features, kMaxOutFeatures))
     return TF_ERR_SHAPE;
   if (!valid_bits(bits)) return TF_ERR_BITS;
-  if (out_dtype != TF_F16 && out_dtype != TF_F32) return TF_ERR_DTYPE;
+  if (out_dtype != TF_F16 && out_dtype != TF_F32 && out_dtype != TF_BF16) return TF_ERR_DTYPE;
   if (rows == 0) return TF_OK;
   if (!xr || !trellis || !svh || !y) return TF_ERR_NULL;
   if (!aligned16(xr) || !aligned16(trellis) || !aligned16(svh) || !aligned16(y)) return TF_ERR_ALIGN;
@@ -220,7 +220,7 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
     p.trellis = static_cast<const uint32_t*>(trellis);
     p.svh = static_cast<const __half*>(svh);
     p.y = static_cast<char*>(y) + static_cast<size_t>(r0) * out_features * out_elem;
-    p.out_f32 = out_dtype == TF_F32 ? 1 : 0;
+    p.out_dtype = out_dtype;
     p.rows = rows - r0 < 16 ? rows - r0 : 16;
     p.in_features = in_features;
     p.out_features = out_features;

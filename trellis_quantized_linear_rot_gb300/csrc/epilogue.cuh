@@ -4,7 +4,8 @@
 // butterflies first, then the scale): for each row, the 128 fp32 K sums of a
 // block go through the seven butterfly stages h = 1..64 (lower <- a + b,
 // upper <- a - b), then are multiplied by fp32 1/sqrt(128), then by fp32 svh,
-// and stored as fp32 or rounded once to fp16.
+// and stored as fp32 or rounded once to fp16 or bf16 (nearest, ties to even;
+// the page's linear registers a 4-bit bf16-output variant beside the fp32 one).
 //
 // Thread n (0..127) of a 128-thread group holds output n of the block for the
 // 16 row slots; stages h = 1..16 are lane shuffles, h = 32 and 64 go through
@@ -12,6 +13,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -67,8 +69,10 @@ __device__ __forceinline__ void store_outputs(const float (&v)[16], const Linear
     if (r < p.rows) {
       const float t = __fmul_rn(__fmul_rn(v[r], kOutRotScale), sv);
       const size_t idx = static_cast<size_t>(r) * p.out_features + o;
-      if (p.out_f32)
+      if (p.out_dtype == TF_F32)
         static_cast<float*>(p.y)[idx] = t;
+      else if (p.out_dtype == TF_BF16)
+        static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(t);
       else
         static_cast<__half*>(p.y)[idx] = __float2half_rn(t);
     }

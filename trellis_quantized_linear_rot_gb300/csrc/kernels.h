@@ -27,7 +27,7 @@ struct LinearPass {
   const uint32_t* trellis;   // packed tiles
   const __half* svh;         // [out]
   void* y;                   // [rows][out]
-  int out_f32;               // 1: fp32 output, 0: fp16
+  int out_dtype;             // TF_F16, TF_F32 or TF_BF16
   int rows;                  // 1..16
   int in_features;
   int out_features;

@@ -83,7 +83,7 @@ struct MmaParams {
   long long units;      // (out/128) * (in/128)
   int units_per_block;  // in / 128
   int ctas;
-  int out_f32;
+  int out_dtype;  // TF_F16, TF_F32 or TF_BF16
   int rows;
   int in_features;
   int out_features;
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     LinearPass lp;
     lp.svh = p.svh;
     lp.y = p.y;
-    lp.out_f32 = p.out_f32;
+    lp.out_dtype = p.out_dtype;
     lp.rows = p.rows;
     lp.in_features = p.in_features;
     lp.out_features = p.out_features;
@@ -608,7 +608,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
   p.units_per_block = lp.in_features / (16 * UKT);
   p.units = static_cast<long long>(lp.out_features / 128) * p.units_per_block;
   p.ctas = ws.ctas;
-  p.out_f32 = lp.out_f32;
+  p.out_dtype = lp.out_dtype;
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;

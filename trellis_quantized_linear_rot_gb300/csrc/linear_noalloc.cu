@@ -55,7 +55,7 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
       out_features <= 0 || out_features % 128)
     return TF_ERR_SHAPE;
   if (!(bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8)) return TF_ERR_BITS;
-  if (out_dtype != TF_F16 && out_dtype != TF_F32) return TF_ERR_DTYPE;
+  if (out_dtype != TF_F16 && out_dtype != TF_F32 && out_dtype != TF_BF16) return TF_ERR_DTYPE;
   if (out_features / 128 > kNoAllocMaxBlocks) return TF_ERR_SCRATCH;
   if (rows == 0) return TF_OK;
   if (!xr || !trellis || !svh || !y) return TF_ERR_NULL;
@@ -100,7 +100,7 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
     p.trellis = static_cast<const uint32_t*>(trellis);
     p.svh = static_cast<const __half*>(svh);
     p.y = static_cast<char*>(y) + static_cast<size_t>(r0) * out_features * out_elem;
-    p.out_f32 = out_dtype == TF_F32 ? 1 : 0;
+    p.out_dtype = out_dtype;
     p.rows = rows - r0 < 16 ? rows - r0 : 16;
     p.in_features = in_features;
     p.out_features = out_features;
