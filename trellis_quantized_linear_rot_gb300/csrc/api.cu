@@ -75,7 +75,7 @@ tf_status ensure_workspace(DeviceCtx* c) {
   const size_t counters = kMaxOutFeatures / 128;
   void* part = nullptr;
   void* cnt = nullptr;
-  cudaError_t e = cudaMalloc(&part, slots * 16 * 128 * sizeof(float));
+  cudaError_t e = cudaMalloc(&part, slots * kMaxPassRows * 128 * sizeof(float));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (workspace)");
   e = cudaMalloc(&cnt, counters * sizeof(int));
   if (e != cudaSuccess) {
@@ -214,14 +214,14 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
   ws.err_flag = ctx->err_flag;
   ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
-  for (int r0 = 0; r0 < rows; r0 += 16) {
+  for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
     LinearPass p;
     p.xr = static_cast<const __half*>(xr) + static_cast<size_t>(r0) * in_features;
     p.trellis = static_cast<const uint32_t*>(trellis);
     p.svh = static_cast<const __half*>(svh);
     p.y = static_cast<char*>(y) + static_cast<size_t>(r0) * out_features * out_elem;
     p.out_dtype = out_dtype;
-    p.rows = rows - r0 < 16 ? rows - r0 : 16;
+    p.rows = rows - r0 < kMaxPassRows ? rows - r0 : kMaxPassRows;
     p.in_features = in_features;
     p.out_features = out_features;
     p.bits = bits;

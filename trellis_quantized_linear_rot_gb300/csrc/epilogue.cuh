@@ -60,15 +60,16 @@ __device__ __forceinline__ void fwht_outputs(float (&v)[16], int rows, int n, fl
   }
 }
 
+// Stores rows row0 .. row0 + 15 of the pass (those below p.rows).
 __device__ __forceinline__ void store_outputs(const float (&v)[16], const LinearPass& p, int blk,
-                                              int n) {
+                                              int n, int row0) {
   const int o = blk * 128 + n;
   const float sv = __half2float(p.svh[o]);
 #pragma unroll
   for (int r = 0; r < 16; ++r) {
-    if (r < p.rows) {
+    if (row0 + r < p.rows) {
       const float t = __fmul_rn(__fmul_rn(v[r], kOutRotScale), sv);
-      const size_t idx = static_cast<size_t>(r) * p.out_features + o;
+      const size_t idx = static_cast<size_t>(row0 + r) * p.out_features + o;
       if (p.out_dtype == TF_F32)
         static_cast<float*>(p.y)[idx] = t;
       else if (p.out_dtype == TF_BF16)
@@ -81,9 +82,21 @@ __device__ __forceinline__ void store_outputs(const float (&v)[16], const Linear
 
 __device__ __forceinline__ void block_epilogue(float (&v)[16], const LinearPass& p, int blk, int n,
                                                float (*xch)[128], int bar_id = 0,
-                                               int nthreads = 128) {
-  fwht_outputs(v, p.rows, n, xch, bar_id, nthreads);
-  store_outputs(v, p, blk, n);
+                                               int nthreads = 128, int row0 = 0) {
+  fwht_outputs(v, p.rows - row0 < 16 ? p.rows - row0 : 16, n, xch, bar_id, nthreads);
+  store_outputs(v, p, blk, n, row0);
+}
+
+// A pass of SLOTS row slots (16 or 32): the rotation and stores run 16 row
+// slots at a time, each row on its own.
+template <int SLOTS>
+__device__ __forceinline__ void block_epilogue_slots(float (&v)[SLOTS], const LinearPass& p, int blk, int n,
+                                                     float (*xch)[128], int bar_id, int nthreads) {
+#pragma unroll
+  for (int h = 0; h < SLOTS; h += 16) {
+    if (h < p.rows)
+      block_epilogue(*reinterpret_cast<float(*)[16]>(&v[h]), p, blk, n, xch, bar_id, nthreads, h);
+  }
 }
 
 }  // namespace tfx

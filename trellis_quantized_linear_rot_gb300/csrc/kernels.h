@@ -21,14 +21,18 @@ cudaError_t launch_rot_in(const void* x, int x_dtype, const __half* suh, __half*
 cudaError_t launch_trellis_decode(const uint32_t* trellis, __half* w, int in_features,
                                   int out_features, int bits, cudaStream_t stream);
 
-// One pass of at most 16 rows through the trellis linear.
+// Rows of one pass of the linear: the weights are decoded once per pass, and
+// each decoded tile feeds the MMAs of all the pass's rows.
+constexpr int kMaxPassRows = 32;
+
+// One pass of at most kMaxPassRows rows through the trellis linear.
 struct LinearPass {
   const __half* xr;          // [rows][in] fp16
   const uint32_t* trellis;   // packed tiles
   const __half* svh;         // [out]
   void* y;                   // [rows][out]
   int out_dtype;             // TF_F16, TF_F32 or TF_BF16
-  int rows;                  // 1..16
+  int rows;                  // 1..kMaxPassRows
   int in_features;
   int out_features;
   int bits;
@@ -57,6 +61,13 @@ struct TcWorkspace {
 };
 
 int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features, int bits);
+// The kernels of one bit width, with ukt k-tiles per unit (8 or 16).
+cudaError_t run_trellis_linear_w2(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
+cudaError_t run_trellis_linear_w3(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
+cudaError_t run_trellis_linear_w4(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
+cudaError_t run_trellis_linear_w5(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
+cudaError_t run_trellis_linear_w6(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
+cudaError_t run_trellis_linear_w8(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt, cudaStream_t s);
 // strips = false: packed tiles in k-tile-major order; true: strips order.
 cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
                                       cudaStream_t stream);
