@@ -166,6 +166,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, dist, device):
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(bytes_per_step, steps, world, ms_total):
+    """Whole-job weight GB/s of N independent replicas: every rank streams the
+    same bytes per step; the job takes the slowest rank's time."""
+    return bytes_per_step * steps * world / (ms_total * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -173,17 +189,17 @@ def dist_env():
     return world, rank, local
 
 
-def oracle_sample(n_blocks, rows_list, k_tiles=IN_F // 16):
+def oracle_sample(n_blocks, rows_list, k_tiles=IN_F // 16, stream=0):
     """The oracle on a bounded sample of the workload: the weights of n_blocks
     output blocks of 128 over the first k_tiles * 16 inputs (decoded from a
-    packed stream of the same distribution), for each row count: rot_in,
-    decode, float64 linear and output rotation. Returns (seconds, packed
-    weight bytes covered)."""
+    packed stream of the same distribution; `stream` picks another seeded
+    stream), for each row count: rot_in, decode, float64 linear and output
+    rotation. Returns (seconds, packed weight bytes covered)."""
     import numpy as np
     from oracle import exl3 as o
     from trellis_quantized_linear_rot_gb300 import synth
     i_s = 128 * max(1, k_tiles // 8)
-    g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS))
+    g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS + 1000 * stream))
     tr = g.integers(0, 2**32, size=i_s * 128 * n_blocks * BITS // 32, dtype=np.uint32)
     x = synth.make_x(max(rows_list), i_s, synth.SEED_X + 2)
     suh = synth.make_scale(i_s, synth.SEED_SUH + 2)
@@ -205,6 +221,45 @@ def cpu_threads():
         return os.cpu_count()
 
 
+def _oracle_job(job):
+    return oracle_sample(*job)
+
+
+class OraclePool:
+    """The oracle on every host core: one worker process per core, started
+    with spawn (never forked from a process that has used the GPU), each with
+    its BLAS limited to one thread, each timing its own seeded sample."""
+
+    ONE_THREAD = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+    def __init__(self, workers):
+        import multiprocessing as mp
+        self.workers = workers
+        saved = {k: os.environ.get(k) for k in self.ONE_THREAD}
+        for k in self.ONE_THREAD:
+            os.environ[k] = "1"
+        try:
+            self.pool = mp.get_context("spawn").Pool(workers)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.run(1, ROWS[:1], 8)  # imports in every worker
+
+    def run(self, n_blocks_each, rows_list, k_tiles):
+        """Wall seconds for all workers' samples, and the bytes they covered."""
+        jobs = [(n_blocks_each, tuple(rows_list), k_tiles, w) for w in range(self.workers)]
+        t0 = time.perf_counter()
+        res = self.pool.map(_oracle_job, jobs)
+        return time.perf_counter() - t0, sum(r[1] for r in res)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
 def run_reference(args):
     """The oracle timed on the host cores, on the same workload and metric.
     Each step is a bounded sample of it (one output block over a slice of the
@@ -213,27 +268,29 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    t_cal, _ = oracle_sample(1, ROWS, k_tiles=8)          # 128 inputs x 128 outputs
+    pool = OraclePool(cpu_threads())
+    t_cal, _ = pool.run(1, ROWS, 8)                    # 128 inputs x 128 outputs per worker
     per_step = 120.0 / max(1, args.steps + args.warmup)
     k_tiles = int(max(8, min(IN_F // 16, 8 * per_step / max(t_cal, 1e-6))))
     for _ in range(args.warmup):
-        oracle_sample(1, ROWS, k_tiles)
+        pool.run(1, ROWS, k_tiles)
     total_t, total_b = 0.0, 0
     for _ in range(args.steps):
-        t, b = oracle_sample(1, ROWS, k_tiles)
+        t, b = pool.run(1, ROWS, k_tiles)
         total_t += t
         total_b += b
+    pool.close()
     value = total_b / total_t / 1e9
-    sample = ("1 of 1010 output blocks over %d of 5120 inputs per row count (rows {1,8,16}) per step"
-              % (128 * max(1, k_tiles // 8)))
+    sample = ("per worker and step: 1 of 1010 output blocks over %d of 5120 inputs per row count "
+              "(rows {1,8,16}); %d single-threaded workers" % (128 * max(1, k_tiles // 8), pool.workers))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F,
                                         "out_features": OUT_F, "bits": BITS},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-                         "host_threads_available": cpu_threads()},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
+                         "sample": sample, "host_threads_available": cpu_threads()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -307,14 +364,10 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier()
     tf.tf_device_error()
-    ms_total = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(stop), dist, dev)
     ms_step = ms_total / args.steps
     bytes_step = weight_bytes() * len(ROWS)
-    value = bytes_step * args.steps * world / (ms_total * 1e-3) / 1e9
+    value = replica_value(bytes_step, args.steps, world, ms_total)
 
     # Dominant kernel: the linear launches, timed by events on their stream.
     per_rows = {}
@@ -355,11 +408,8 @@ def run_ours(args):
         for _ in range(e2e_steps):
             e2e_step()
         e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = bytes_step * e2e_steps * world / e2e_s / 1e9 if not args.no_e2e else None
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
+    e2e_value = replica_value(bytes_step, e2e_steps, world, e2e_s * 1e3) if not args.no_e2e else None
 
     if rank != 0:
         if dist is not None:
@@ -368,11 +418,13 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_blocks = 120
-        secs, covered = oracle_sample(n_blocks, ROWS)
-        cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": "%d of 1010 output blocks (5120x128 weights each) for each of rows {1,8,16}, "
-                         "%.1f s" % (n_blocks, secs),
+        n_blocks = 60
+        pool = OraclePool(cpu_threads())
+        secs, covered = pool.run(n_blocks, ROWS, IN_F // 16)
+        pool.close()
+        cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
+               "sample": "per worker: %d of 1010 output blocks (5120x128 weights each) for each of rows "
+                         "{1,8,16}; %d single-threaded workers, %.1f s wall" % (n_blocks, pool.workers, secs),
                "host_threads_available": cpu_threads()}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
