@@ -241,6 +241,42 @@ def test_non_finite_classes_match_float64():
     assert np.array_equal(np.isneginf(y), np.isneginf(ref))
 
 
+# -------------------------------------------------------------- maximum sizes
+def test_max_in_features_one_block_across_every_cta():
+    """in = 2^20 (the largest accepted), out = 128, 3 rows, 4 bits: the one
+    output block is cut between every CTA of the launch, whose partial sums
+    the last arriver adds in CTA order. Each row of xr is zero except at 96
+    random inputs spread over the whole range (and the first and last), so
+    every CTA's part carries terms while the float64 reference needs only
+    those weight rows; the kernel still streams and decodes all weights."""
+    i_f, o_f, bits, rows = 1 << 20, 128, 4, 3
+    g = np.random.Generator(np.random.PCG64(4321))
+    tr = synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + 30 + bits)
+    svh = synth.make_scale(o_f, synth.SEED_SVH + 30)
+    xr = np.zeros((rows, i_f), np.float16)
+    ks = np.unique(np.concatenate([[0, i_f - 1], g.integers(0, i_f, size=96)]))
+    for r in range(rows):
+        xr[r, ks] = g.standard_normal(ks.size).astype(np.float16)
+    y = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    # The zero inputs add nothing: the reference is the oracle's linear over
+    # the chosen inputs and their decoded weight rows.
+    ref = o.linear_f64(xr[:, ks], o.decode_rows(tr, i_f, o_f, bits, ks), svh)
+    assert_close_f32(y, ref)
+
+
+def test_max_out_features_sampled():
+    """out = 2^24 (the largest accepted), in = 128, 1 row, 2 bits, fp16 out:
+    131,072 output blocks; sampled blocks at both ends and the middle."""
+    i_f, o_f, bits = 128, 1 << 24, 2
+    x, suh, svh, tr = inputs(1, i_f, o_f, bits, c=31)
+    xr = o.rot_in_f32(x, suh)
+    y = run_linear(xr, tr, svh, bits, o_f, torch.float16)
+    blocks = [0, 65536, (o_f // 128) - 1]
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(xr, o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f16(y[:, cols], ref)
+
+
 # ------------------------------------------------------------ strips layout
 @pytest.mark.parametrize("bits", o.BITS_ALLOWED)
 def test_to_strips_matches_oracle_order(bits):
