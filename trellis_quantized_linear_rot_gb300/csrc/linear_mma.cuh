@@ -83,7 +83,9 @@ struct Cfg {
   static constexpr int kDbufBytes = 2 * kGroups * kSlots * 128 * 4;  // [2][groups][slots][128] fp32
   static constexpr int kBudget = NB <= 2 ? kSmemBudget : kSmemBudgetWide;
   static constexpr int kStagesFit = (kBudget - kDbufBytes - 8192 - 1024) / kStageBytes;
-  static constexpr int kStages = kStagesFit < 12 ? kStagesFit : 12;
+  // Even, so that unit k and unit k - kStages (the stage's previous unit)
+  // always belong to the same compute group (see the kernel).
+  static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) & ~1;
 };
 
 struct MmaParams {
@@ -294,6 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<BITS, UKT, NB>;
   constexpr int kSlots = C::kSlots;
   constexpr int S = L::kStages;
+  // Unit k (processing position) sits in stage k % S, phase k / S, and goes
+  // to compute group k % 2. With S even, a stage's previous unit k - S went
+  // to the same group, which therefore read it (so its phase completed)
+  // before it waits for unit k: no wait can look two phases ahead, where a
+  // parity test could not tell the phases apart.
+  static_assert(S % kGroups == 0 && S >= 2 * kGroups, "a stage must stay with one compute group");
   extern __shared__ __align__(1024) uint8_t smem[];
   float* dbuf = reinterpret_cast<float*>(smem + L::kDbufOff);
   float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + L::kXchOff);
@@ -411,7 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float d[NB][4];  // row slots 8q .. 8q+7
 #pragma unroll
       for (int q = 0; q < NB; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-      int i = seg_lo + ((cg - seg_lo) % kGroups + kGroups) % kGroups;
+      // The group's units of the segment: processing positions k = base + i
+      // with k % 2 == cg, in order.
+      int i = seg_lo + (((cg - base - seg_lo) % kGroups) + kGroups) % kGroups;
       for (; i < seg_hi; i += kGroups) {
         const int k = base + i;
         const int s = k % S;
