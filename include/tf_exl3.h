@@ -168,6 +168,18 @@ tf_status tf_trellis_linear_noalloc(const void* xr, const void* trellis, const v
 tf_status tf_trellis_decode(const void* trellis, void* w, int in_features,
                             int out_features, int bits, void* stream);
 
+/*
+ * tf_selftest_stranded_wait -- a self-test of the failure path every kernel
+ * of this library has: launches, on `stream`, one tiny kernel whose
+ * shared-memory barrier wait is never completed. The wait gives up after the
+ * library's bounded-wait limit (1 s of GPU time), records that in the
+ * device error flag and returns; the next tf_device_error(stream) returns
+ * TF_ERR_TIMEOUT and clears the flag, and the CUDA context stays usable.
+ * The pages have no counterpart (their planted faults run on the host).
+ * Returns TF_OK when the kernel was launched.
+ */
+tf_status tf_selftest_stranded_wait(void* stream);
+
 /* Bytes of a packed trellis: in_features * out_features * bits / 8, or 0 for
  * an invalid shape or width. */
 size_t tf_trellis_bytes(int in_features, int out_features, int bits);

@@ -351,3 +351,22 @@ def test_host_pointer_is_refused():
         tf.tf_trellis_linear(xr, dev(synth.make_trellis(512, 128, 4, 1)), dev(synth.make_scale(128, 2)),
                              4, 128, y=torch.empty((1, 128), device="cuda"))
     assert e.value.status == tf.TF_ERR_POINTER
+
+
+# ------------------------------------------------------------- failure path
+def test_stranded_wait_reports_timeout_and_context_survives():
+    """A kernel whose barrier wait nothing completes gives up after the
+    bounded-wait limit, the host reads TF_ERR_TIMEOUT, and the context goes
+    on working (a linear right after it matches the oracle)."""
+    tf.tf_device_error()
+    tf.tf_selftest_stranded_wait()
+    with pytest.raises(tf.TFError) as err:
+        tf.tf_device_error()
+    assert err.value.status == tf.TF_ERR_TIMEOUT
+    tf.tf_device_error()  # the record was cleared
+    i_f, o_f, bits = 384, 256, 4
+    x, suh, svh, tr = inputs(2, i_f, o_f, bits, c=40)
+    xr = o.rot_in_f32(x, suh)
+    y = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    tf.tf_device_error()
+    assert_close_f32(y, o.linear_f64(xr, o.decode_matrix(tr, i_f, o_f, bits), svh))

@@ -32,6 +32,7 @@ SIGNATURES = {
     "tf_status_string": (ctypes.c_char_p, [_I]),
     "tf_last_error": (ctypes.c_char_p, []),
     "tf_device_error": (_I, [_VP]),
+    "tf_selftest_stranded_wait": (_I, [_VP]),
 }
 
 _lib = None
@@ -185,6 +186,11 @@ def tf_trellis_decode(trellis, in_features, out_features, bits, w=None, stream=N
     st = lib().tf_trellis_decode(_ptr(trellis), _ptr(w), in_features, out_features, bits, _stream(stream))
     _check(st, "tf_trellis_decode")
     return w
+
+
+def tf_selftest_stranded_wait(stream=None):
+    """Launches the failure-path self-test (see tf_selftest_stranded_wait)."""
+    _check(lib().tf_selftest_stranded_wait(_stream(stream)), "tf_selftest_stranded_wait")
 
 
 def tf_device_error(stream=None):

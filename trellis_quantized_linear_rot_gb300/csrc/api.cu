@@ -282,6 +282,15 @@ tf_status tf_trellis_decode(const void* trellis, void* w, int in_features, int o
   return TF_OK;
 }
 
+tf_status tf_selftest_stranded_wait(void* stream) {
+  DeviceCtx* ctx = nullptr;
+  tf_status s = current_ctx(&ctx);
+  if (s != TF_OK) return s;
+  cudaError_t e = launch_stranded_wait(ctx->err_flag, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stranded-wait self-test launch");
+  return TF_OK;
+}
+
 tf_status tf_device_error(void* stream) {
   DeviceCtx* ctx = nullptr;
   tf_status s = current_ctx(&ctx);

@@ -71,6 +71,8 @@ cudaError_t run_trellis_linear_w8(const LinearPass& p, const TcWorkspace& ws, bo
 // strips = false: packed tiles in k-tile-major order; true: strips order.
 cudaError_t launch_trellis_linear_mma(const LinearPass& p, const TcWorkspace& ws, bool strips,
                                       cudaStream_t stream);
+// One bounded barrier wait that nothing completes (the failure-path self-test).
+cudaError_t launch_stranded_wait(int* err_flag, cudaStream_t stream);
 cudaError_t launch_tiles_to_strips(const uint32_t* tiles, uint32_t* strips, int in_features,
                                    int out_features, int bits, cudaStream_t stream);
 
