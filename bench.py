@@ -386,10 +386,14 @@ def run_ours(args):
     alu_peak = alu_peak_tops(num_sms)
     alu_achieved = IN_F * OUT_F * DECODE_OPS_PER_WEIGHT * launches / (dur_sum * 1e-3) / 1e12
 
-    # End to end through the public API from pinned host memory.
+    # End to end through the public API from pinned host memory: every call
+    # copies its rows of x in, and its logits out on a copy stream that waits
+    # for the call, so that the read of one call's logits overlaps the next
+    # call; the timed region ends when every copy has landed.
     x_host = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).pin_memory()
     y_host = {r: torch.empty((r, OUT_F), dtype=torch.float32).pin_memory() for r in ROWS}
-    e2e_steps = max(2, min(args.steps, 10))
+    e2e_steps = max(2, min(args.steps, 200))
+    copy_stream = torch.cuda.Stream(device=dev)
 
     def e2e_step():
         for r in ROWS:
@@ -397,16 +401,22 @@ def run_ours(args):
             xr = tf.tf_rot_in(xd, suh)
             y = linear(xr, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
             call[0] += 1
-            y_host[r].copy_(y, non_blocking=True)
-        torch.cuda.synchronize()
+            done = torch.cuda.Event()
+            done.record(stream)
+            copy_stream.wait_event(done)
+            with torch.cuda.stream(copy_stream):
+                y_host[r].copy_(y, non_blocking=True)
+            y.record_stream(copy_stream)
 
     e2e_s = float("nan")
     if not args.no_e2e:
         e2e_step()
+        torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
+        torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, dist, dev)
     e2e_value = replica_value(bytes_step, e2e_steps, world, e2e_s * 1e3) if not args.no_e2e else None
