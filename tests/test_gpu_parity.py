@@ -286,7 +286,8 @@ def test_to_strips_matches_oracle_order(bits):
     assert np.array_equal(got, o.tiles_to_strips(tr, i_f, o_f, bits))
 
 
-@pytest.mark.parametrize("bits,rows", [(4, 1), (4, 16), (6, 9), (8, 3), (3, 16), (2, 5), (5, 12)])
+@pytest.mark.parametrize("bits,rows", [(4, 1), (4, 16), (6, 9), (8, 3), (3, 16), (2, 5), (5, 12),
+                                       (4, 32), (6, 24), (2, 17), (8, 29), (5, 40)])
 def test_linear_strips_equals_tiles_bit_for_bit(bits, rows):
     """The strips order streams the same tiles: outputs are identical bits,
     and match the oracle (sampled) on the wkv shape."""
@@ -304,23 +305,29 @@ def test_linear_strips_equals_tiles_bit_for_bit(bits, rows):
 
 
 # ------------------------------------------------------- GPU-vs-GPU invariants
-def test_row_independence_windows_and_passes():
-    """LM head 5120 -> 129,280 at 6 bits, 64 rows as four passes of 16: every
+@pytest.mark.parametrize("layout", ["tiles", "strips"])
+def test_row_independence_windows_and_passes(layout):
+    """LM head 5120 -> 129,280 at 6 bits, 64 rows as two passes of 32: every
     row's outputs equal its single-row run bit for bit, also inside random
-    windows of 2 to 24 rows ("Checks on this head", the window test)."""
+    windows of 2 to 24 rows ("Checks on this head", the window test), in
+    both weight orders."""
     i_f, o_f, bits, rows = 5120, 129280, 6, 64
     x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=5)
     tr_t, svh_t = dev(tr), dev(svh)
+    lin = tf.tf_trellis_linear
+    if layout == "strips":
+        tr_t = tf.tf_trellis_to_strips(tr_t, i_f, o_f, bits)
+        lin = tf.tf_trellis_linear_strips
     xr_t = tf.tf_rot_in(dev(x), dev(suh))
-    full = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+    full = host(lin(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
     singles = {}
     for r in range(rows):
-        singles[r] = host(tf.tf_trellis_linear(xr_t[r:r + 1], tr_t, svh_t, bits, o_f,
-                                               out_dtype=torch.float32)).view(np.uint32)[0]
+        singles[r] = host(lin(xr_t[r:r + 1], tr_t, svh_t, bits, o_f,
+                              out_dtype=torch.float32)).view(np.uint32)[0]
         assert np.array_equal(full[r], singles[r]), "row %d differs in the 64-row launch" % r
     for first, n in synth.random_windows(rows, 50, seed=55):
-        win = host(tf.tf_trellis_linear(xr_t[first:first + n], tr_t, svh_t, bits, o_f,
-                                        out_dtype=torch.float32)).view(np.uint32)
+        win = host(lin(xr_t[first:first + n], tr_t, svh_t, bits, o_f,
+                       out_dtype=torch.float32)).view(np.uint32)
         for j in range(n):
             assert np.array_equal(win[j], singles[first + j]), "window (%d, %d) row %d" % (first, n, j)
     blocks = [2, 700]
