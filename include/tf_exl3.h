@@ -43,7 +43,7 @@ typedef enum {
   TF_ERR_CUDA = 6,     /* a CUDA runtime call or launch failed (tf_last_error) */
   TF_ERR_TIMEOUT = 7,  /* a kernel's bounded wait expired (tf_device_error)    */
   TF_ERR_POINTER = 8,  /* a pointer is not device memory of the current device */
-  TF_ERR_SCRATCH = 9   /* the problem needs more scratch than tf_trellis_linear_noalloc holds */
+  TF_ERR_SCRATCH = 9   /* the problem needs more scratch than the given workspace or the no-allocation array holds */
 } tf_status;
 
 typedef enum { TF_F16 = 0, TF_F32 = 1, TF_BF16 = 2 } tf_dtype;
@@ -135,6 +135,34 @@ tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const voi
  */
 tf_status tf_trellis_to_strips(const void* tiles, void* strips, int in_features,
                                int out_features, int bits, void* stream);
+
+/*
+ * tf_trellis_workspace_bytes -- bytes of caller workspace tf_trellis_linear_ws
+ * needs for this shape on the current device (it depends on the device's SM
+ * count), or 0 for an invalid shape or width, or when no device is usable.
+ */
+size_t tf_trellis_workspace_bytes(int in_features, int out_features, int bits);
+
+/*
+ * tf_trellis_linear_ws -- tf_trellis_linear (layout 0: the k-tile-major
+ * tiles) or tf_trellis_linear_strips (layout 1: the strips order) with the
+ * scratch in caller memory instead of the library's per-device workspace,
+ * so that calls with distinct workspaces may run at the same time on
+ * different streams of one device. The pages have no counterpart (they
+ * describe one call at a time).
+ * workspace: device memory of the current device, 256-byte aligned, at least
+ *   tf_trellis_workspace_bytes(in_features, out_features, bits) bytes, owned
+ *   by the caller; each call clears the part it counts arrivals in with
+ *   cudaMemsetAsync on `stream`, so it needs no initialisation. Calls that
+ *   share one workspace must be ordered by the caller.
+ * Same results (bit for bit) as the entry points above; refusals as theirs,
+ * plus TF_ERR_SHAPE for a layout other than 0 or 1, TF_ERR_NULL / TF_ERR_ALIGN
+ * for the workspace, and TF_ERR_SCRATCH when workspace_bytes is too small.
+ */
+tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* svh,
+                               void* y, int out_dtype, int rows, int in_features,
+                               int out_features, int bits, int layout, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * tf_trellis_linear_noalloc -- the same computation as tf_trellis_linear

@@ -86,6 +86,20 @@ def test_linear_refusals(lib):
     assert lin(lib, rows=0, xr=NUL, y=NUL) == tf.TF_OK
 
 
+def test_linear_ws_refusals(lib):
+    f = lib.tf_trellis_linear_ws
+    def ws(layout=0, work=P, rows=1, i=512, bits=4, dt=tf.TF_F32):
+        return f(P, P, P, P, dt, rows, i, 128, bits, layout, work, 1 << 20, S)
+    assert ws(layout=2) == tf.TF_ERR_SHAPE
+    assert ws(i=500) == tf.TF_ERR_SHAPE
+    assert ws(bits=7) == tf.TF_ERR_BITS
+    assert ws(dt=5) == tf.TF_ERR_DTYPE
+    assert ws(work=NUL) == tf.TF_ERR_NULL
+    assert ws(work=ctypes.c_void_p(0x10010)) == tf.TF_ERR_ALIGN   # 16-byte aligned only
+    assert ws(rows=0, work=NUL) == tf.TF_OK
+    assert lib.tf_trellis_workspace_bytes(500, 128, 4) == 0
+
+
 def test_rot_in_refusals(lib):
     f = lib.tf_rot_in
     assert f(P, tf.TF_F16, P, P, -1, 512, S) == tf.TF_ERR_SHAPE

@@ -360,6 +360,41 @@ def test_host_pointer_is_refused():
     assert e.value.status == tf.TF_ERR_POINTER
 
 
+# ------------------------------------------------------------ caller workspace
+def test_linear_ws_concurrent_streams_match_serial_calls():
+    """Two calls on two streams at once, each with its own workspace, give the
+    same bits as tf_trellis_linear one after the other (tiles and strips); a
+    workspace one byte short is refused."""
+    i_f, o_f, bits = 6144, 25600, 4
+    xa, suh, svh, tr = inputs(3, i_f, o_f, bits, c=50)
+    xb = synth.make_x(20, i_f, 51)
+    tr_t, svh_t = dev(tr), dev(svh)
+    st_t = tf.tf_trellis_to_strips(tr_t, i_f, o_f, bits)
+    xra = tf.tf_rot_in(dev(xa), dev(suh))
+    xrb = tf.tf_rot_in(dev(xb), dev(suh))
+    ref_a = host(tf.tf_trellis_linear(xra, tr_t, svh_t, bits, o_f, out_dtype=torch.float32))
+    ref_b = host(tf.tf_trellis_linear(xrb, tr_t, svh_t, bits, o_f, out_dtype=torch.float32))
+    need = tf.tf_trellis_workspace_bytes(i_f, o_f, bits)
+    assert need > 0
+    wa = torch.empty(need, dtype=torch.uint8, device="cuda")
+    wb = torch.empty(need, dtype=torch.uint8, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for layout, w in (("tiles", tr_t), ("strips", st_t)):
+        ya = torch.empty((3, o_f), dtype=torch.float32, device="cuda")
+        yb = torch.empty((20, o_f), dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            tf.tf_trellis_linear_ws(xra, w, svh_t, bits, o_f, wa, layout=layout, y=ya, stream=sa)
+            tf.tf_trellis_linear_ws(xrb, w, svh_t, bits, o_f, wb, layout=layout, y=yb, stream=sb)
+        torch.cuda.synchronize()
+        tf.tf_device_error()
+        assert np.array_equal(host(ya).view(np.uint32), ref_a.view(np.uint32))
+        assert np.array_equal(host(yb).view(np.uint32), ref_b.view(np.uint32))
+    with pytest.raises(tf.TFError) as err:
+        tf.tf_trellis_linear_ws(xra, tr_t, svh_t, bits, o_f, wa[:need - 1])
+    assert err.value.status == tf.TF_ERR_SCRATCH
+
+
 # ------------------------------------------------------------- failure path
 def test_stranded_wait_reports_timeout_and_context_survives():
     """A kernel whose barrier wait nothing completes gives up after the

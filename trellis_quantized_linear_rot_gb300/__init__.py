@@ -27,6 +27,8 @@ SIGNATURES = {
     "tf_trellis_linear_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_strips": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_to_strips": (_I, [_VP, _VP, _I, _I, _I, _VP]),
+    "tf_trellis_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "tf_trellis_linear_ws": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     "tf_trellis_decode": (_I, [_VP, _VP, _I, _I, _I, _VP]),
     "tf_trellis_bytes": (_SZ, [_I, _I, _I]),
     "tf_status_string": (ctypes.c_char_p, [_I]),
@@ -162,6 +164,29 @@ def tf_trellis_linear_strips(xr, strips, svh, bits, out_features, out_dtype=None
     st = lib().tf_trellis_linear_strips(_ptr(xr), _ptr(strips), _ptr(svh), _ptr(y), _dtype_code(y.dtype),
                                         rows, in_f, out_features, bits, _stream(stream))
     _check(st, "tf_trellis_linear_strips")
+    return y
+
+
+def tf_trellis_workspace_bytes(in_features, out_features, bits):
+    return lib().tf_trellis_workspace_bytes(in_features, out_features, bits)
+
+
+def tf_trellis_linear_ws(xr, trellis, svh, bits, out_features, workspace, layout="tiles", out_dtype=None,
+                         y=None, stream=None):
+    """The trellis linear with its scratch in `workspace` (a CUDA tensor of at
+    least tf_trellis_workspace_bytes bytes); layout "tiles" or "strips"."""
+    import torch
+    rows, in_f = xr.shape
+    for t, n in ((xr, "xr"), (trellis, "trellis"), (svh, "svh"), (workspace, "workspace")):
+        _contig(t, n)
+    if y is None:
+        y = torch.empty((rows, out_features), dtype=out_dtype or torch.float32, device=xr.device)
+    _contig(y, "y")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib().tf_trellis_linear_ws(_ptr(xr), _ptr(trellis), _ptr(svh), _ptr(y), _dtype_code(y.dtype), rows,
+                                    in_f, out_features, bits, {"tiles": 0, "strips": 1}[layout],
+                                    _ptr(workspace), nbytes, _stream(stream))
+    _check(st, "tf_trellis_linear_ws")
     return y
 
 

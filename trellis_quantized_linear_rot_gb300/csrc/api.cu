@@ -157,7 +157,7 @@ const char* tf_status_string(int status) {
     case TF_ERR_CUDA: return "a CUDA call failed (see tf_last_error)";
     case TF_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     case TF_ERR_POINTER: return "a pointer is not device memory of the current device";
-    case TF_ERR_SCRATCH: return "the problem needs more scratch than the fixed no-allocation array holds";
+    case TF_ERR_SCRATCH: return "the problem needs more scratch than the given workspace or the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }
@@ -243,6 +243,71 @@ tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const voi
                                    int bits, void* stream) {
   return linear_entry(xr, strips, svh, y, out_dtype, rows, in_features, out_features, bits, true,
                       stream);
+}
+
+// Caller workspace of tf_trellis_linear_ws: partial sums for every CTA of a
+// launch ([ctas][2][kMaxPassRows][128] fp32), then one arrival counter per
+// output block, each part starting on a 256-byte boundary.
+static size_t ws_partial_bytes(int ctas) {
+  const size_t b = static_cast<size_t>(ctas) * 2 * kMaxPassRows * 128 * sizeof(float);
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+
+size_t tf_trellis_workspace_bytes(int in_features, int out_features, int bits) {
+  if (!valid_features(in_features, kMaxInFeatures) || !valid_features(out_features, kMaxOutFeatures) ||
+      !valid_bits(bits))
+    return 0;
+  DeviceCtx* ctx = nullptr;
+  if (current_ctx(&ctx) != TF_OK) return 0;
+  const int ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
+  return ws_partial_bytes(ctas) + static_cast<size_t>(out_features / 128) * sizeof(int);
+}
+
+tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* svh, void* y, int out_dtype,
+                               int rows, int in_features, int out_features, int bits, int layout,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  if (rows < 0 || !valid_features(in_features, kMaxInFeatures) ||
+      !valid_features(out_features, kMaxOutFeatures) || (layout != 0 && layout != 1))
+    return TF_ERR_SHAPE;
+  if (!valid_bits(bits)) return TF_ERR_BITS;
+  if (out_dtype != TF_F16 && out_dtype != TF_F32 && out_dtype != TF_BF16) return TF_ERR_DTYPE;
+  if (rows == 0) return TF_OK;
+  if (!xr || !trellis || !svh || !y || !workspace) return TF_ERR_NULL;
+  if (!aligned16(xr) || !aligned16(trellis) || !aligned16(svh) || !aligned16(y) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return TF_ERR_ALIGN;
+  DeviceCtx* ctx = nullptr;
+  tf_status s = current_ctx(&ctx);
+  if (s != TF_OK) return s;
+  s = check_device_ptrs(ctx->device, xr, trellis, svh, y, workspace);
+  if (s != TF_OK) return s;
+  TcWorkspace ws;
+  ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
+  const size_t part = ws_partial_bytes(ws.ctas);
+  if (workspace_bytes < part + static_cast<size_t>(out_features / 128) * sizeof(int)) return TF_ERR_SCRATCH;
+  ws.partials = static_cast<float*>(workspace);
+  ws.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + part);
+  ws.err_flag = ctx->err_flag;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The counters must start at zero; clear the ones this call uses on its stream.
+  cudaError_t e = cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(out_features / 128) * sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (workspace counters)");
+  const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
+  for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
+    LinearPass p;
+    p.xr = static_cast<const __half*>(xr) + static_cast<size_t>(r0) * in_features;
+    p.trellis = static_cast<const uint32_t*>(trellis);
+    p.svh = static_cast<const __half*>(svh);
+    p.y = static_cast<char*>(y) + static_cast<size_t>(r0) * out_features * out_elem;
+    p.out_dtype = out_dtype;
+    p.rows = rows - r0 < kMaxPassRows ? rows - r0 : kMaxPassRows;
+    p.in_features = in_features;
+    p.out_features = out_features;
+    p.bits = bits;
+    e = launch_trellis_linear_mma(p, ws, layout == 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "trellis linear (caller workspace) launch");
+  }
+  return TF_OK;
 }
 
 tf_status tf_trellis_to_strips(const void* tiles, void* strips, int in_features, int out_features,
