@@ -2,7 +2,7 @@
 
 Each translation unit compiles in its own nvcc process (in parallel), then
 one nvcc call links the shared library. The CUDA runtime is linked
-statically; the driver's tensor-map encoder is looked up at run time, so no
+statically; the CUDA driver's tensor-map encoder is looked up at run time, so no
 libcuda link is needed.
 """
 
