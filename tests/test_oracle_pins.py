@@ -523,3 +523,24 @@ def test_bf16_rounding_matches_torch():
     v = v[~np.isnan(v)]
     want = torch.from_numpy(v.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(o.bf16_bits_rne(v), want)
+
+
+def test_epilogue_f32_within_fp32_bound_of_float64():
+    """The fp32-step output epilogue against the float64 one on random sums:
+    7 butterfly stages and two multiplies, each rounding at most half an
+    fp32 ulp, so |y32 - y64| <= 9 * 2^-24 * 128 * max|acc| * s * |svh| per
+    block. A wrong sign, scale, index or dropped term is far outside it."""
+    g = np.random.Generator(np.random.PCG64(77))
+    acc = g.standard_normal((3, 384)).astype(np.float32) * np.float32(1000.0)
+    svh = synth.make_scale(384, 78)
+    y32 = o.epilogue_f32(acc, svh).astype(np.float64)
+    y64 = o.fwht128_f64(acc.astype(np.float64).reshape(3, 3, 128)).reshape(3, 384) / np.sqrt(128.0)
+    y64 = y64 * svh.astype(np.float64)
+    amax = np.abs(acc.astype(np.float64)).reshape(3, 3, 128).max(axis=2)          # per block
+    bound = 9 * 2.0 ** -24 * 128 * amax / np.sqrt(128.0)
+    bound = np.repeat(bound, 128, axis=1) * np.abs(svh.astype(np.float64))
+    assert np.all(np.abs(y32 - y64) <= bound)
+    # and the bound is tight enough to see a one-element slip
+    bad = acc.copy()
+    bad[0, 5] += np.float32(1.0)
+    assert not np.all(np.abs(o.epilogue_f32(bad, svh).astype(np.float64) - y64) <= bound)
