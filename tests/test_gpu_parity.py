@@ -360,6 +360,53 @@ def test_host_pointer_is_refused():
     assert e.value.status == tf.TF_ERR_POINTER
 
 
+# ------------------------------------------------------------- prompt passes
+@pytest.mark.parametrize("bits,rows,layout", [(4, 33, "tiles"), (4, 128, "strips"), (6, 100, "tiles"),
+                                              (2, 129, "strips"), (8, 64, "strips"), (3, 200, "tiles"),
+                                              (5, 96, "strips")])
+def test_prompt_pass_rows_bit_equal_to_decode_rows(bits, rows, layout):
+    """Passes of 33 to 128 rows (the tcgen05 kernel) give every row the same
+    bits as its run alone and as its 16-row pass (the mma.sync kernel), and
+    match the oracle; wkv shape 6144 -> 25,600."""
+    i_f, o_f = 6144, 25600
+    x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=60 + bits)
+    tr_t, svh_t = dev(tr), dev(svh)
+    lin = tf.tf_trellis_linear
+    if layout == "strips":
+        tr_t = tf.tf_trellis_to_strips(tr_t, i_f, o_f, bits)
+        lin = tf.tf_trellis_linear_strips
+    xr_t = tf.tf_rot_in(dev(x), dev(suh))
+    full = host(lin(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+    for r0 in range(0, rows, 16):
+        part = host(lin(xr_t[r0:r0 + 16], tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+        assert np.array_equal(full[r0:r0 + 16], part), "rows %d.. differ from their 16-row pass" % r0
+    for r in (0, rows // 2, rows - 1):
+        one = host(lin(xr_t[r:r + 1], tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+        assert np.array_equal(full[r], one[0])
+    blocks = [0, 123, 199]
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    ref = o.linear_f64(host(xr_t), o.decode_blocks(tr, i_f, o_f, bits, blocks), svh[cols])
+    assert_close_f32(full.view(np.float32)[:, cols], ref)
+
+
+def test_prompt_pass_low_precision_outputs_and_identity():
+    """A 48-row pass with fp16 and bf16 outputs equals the oracle's rounding of
+    its own fp32 output; identity rows are the decoded weight rows' epilogue,
+    bit for bit."""
+    i_f, o_f, bits, rows = 6144, 25600, 4, 48
+    tr = synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + 70)
+    svh = synth.make_scale(o_f, synth.SEED_SVH + 70)
+    ks = synth.identity_ks(rows, i_f)
+    xr = synth.make_identity_rows(rows, i_f, ks)
+    want32 = o.epilogue_f32(o.decode_rows(tr, i_f, o_f, bits, ks).astype(np.float32), svh)
+    y32 = run_linear(xr, tr, svh, bits, o_f, torch.float32)
+    assert np.array_equal(y32.view(np.uint32), want32.view(np.uint32))
+    y16 = run_linear(xr, tr, svh, bits, o_f, torch.float16)
+    assert np.array_equal(bits16(y16), bits16(want32.astype(np.float16)))
+    ybf = run_linear(xr, tr, svh, bits, o_f, torch.bfloat16)
+    assert np.array_equal(ybf, o.bf16_bits_rne(want32))
+
+
 # ------------------------------------------------------------ caller workspace
 def test_linear_ws_concurrent_streams_match_serial_calls():
     """Two calls on two streams at once, each with its own workspace, give the

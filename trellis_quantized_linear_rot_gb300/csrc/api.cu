@@ -71,11 +71,11 @@ tf_status current_ctx(DeviceCtx** out) {
 tf_status ensure_workspace(DeviceCtx* c) {
   std::lock_guard<std::mutex> lock(g_ctx_mutex);
   if (c->partials != nullptr) return TF_OK;
-  const size_t slots = static_cast<size_t>(c->num_sms) * 2;
+  const size_t slots = static_cast<size_t>(c->num_sms);
   const size_t counters = kMaxOutFeatures / 128;
   void* part = nullptr;
   void* cnt = nullptr;
-  cudaError_t e = cudaMalloc(&part, slots * kMaxPassRows * 128 * sizeof(float));
+  cudaError_t e = cudaMalloc(&part, slots * kPartialFloatsPerCta * sizeof(float));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc (workspace)");
   e = cudaMalloc(&cnt, counters * sizeof(int));
   if (e != cudaSuccess) {
@@ -246,10 +246,10 @@ tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const voi
 }
 
 // Caller workspace of tf_trellis_linear_ws: partial sums for every CTA of a
-// launch ([ctas][2][kMaxPassRows][128] fp32), then one arrival counter per
+// launch (kPartialFloatsPerCta fp32 each), then one arrival counter per
 // output block, each part starting on a 256-byte boundary.
 static size_t ws_partial_bytes(int ctas) {
-  const size_t b = static_cast<size_t>(ctas) * 2 * kMaxPassRows * 128 * sizeof(float);
+  const size_t b = static_cast<size_t>(ctas) * kPartialFloatsPerCta * sizeof(float);
   return (b + 255) & ~static_cast<size_t>(255);
 }
 

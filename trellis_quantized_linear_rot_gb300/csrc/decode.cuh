@@ -161,6 +161,30 @@ __device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWor
   }
 }
 
+// The same words from a tile whose consecutive words sit STRIDE words apart
+// (the strips order interleaves the words of four k-tiles).
+template <int BITS, int STRIDE>
+__device__ __forceinline__ void load_col_words_strided(const uint32_t* tw, int n, ColWords<BITS>& cw) {
+  if constexpr (BITS == 4) {
+    cw.w[0] = tw[((2 * n + 31) & 31) * STRIDE];
+    cw.w[1] = tw[(2 * n) * STRIDE];
+    cw.w[2] = tw[(2 * n + 1) * STRIDE];
+  } else if constexpr (BITS == 8) {
+    cw.w[0] = tw[((4 * n + 63) & 63) * STRIDE];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cw.w[1 + j] = tw[(4 * n + j) * STRIDE];
+  } else {
+    using S = RowSpan<BITS>;
+    const int w0 = row_first_bit<BITS>(n) >> 5;
+#pragma unroll
+    for (int j = 0; j < S::kWords; ++j) {
+      int wi = w0 + j;
+      wi = (wi >= S::kTileWords) ? wi - S::kTileWords : wi;
+      cw.w[j] = tw[wi * STRIDE];
+    }
+  }
+}
+
 template <int BITS>
 __device__ __forceinline__ void decode_col_words(const ColWords<BITS>& cw, int n, uint32_t (&out)[8]) {
   if constexpr (BITS == 4) {

@@ -1,11 +1,13 @@
 // The trellis linear's kernels at 2 bits per weight (one translation unit
 // per width so that the widths compile in parallel).
-#include "linear_mma.cuh"
+#include "linear_tc.cuh"
 
 namespace tfx {
 
 cudaError_t run_trellis_linear_w2(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt,
                                   cudaStream_t stream) {
+  if (p.rows > kMaxDecodePassRows)
+    return ukt == 16 ? run_tc<2, 16>(p, ws, strips, stream) : run_tc<2, 8>(p, ws, strips, stream);
   return ukt == 16 ? run_mma<2, 16>(p, ws, strips, stream) : run_mma<2, 8>(p, ws, strips, stream);
 }
 

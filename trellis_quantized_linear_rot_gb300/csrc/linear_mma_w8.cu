@@ -1,13 +1,14 @@
 // The trellis linear's kernels at 8 bits per weight (one translation unit
 // per width so that the widths compile in parallel).
-#include "linear_mma.cuh"
+#include "linear_tc.cuh"
 
 namespace tfx {
 
 cudaError_t run_trellis_linear_w8(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt,
                                   cudaStream_t stream) {
   // Units of 8 k-tiles at this width (16 only up to 5 bits).
-  return ukt == 8 ? run_mma<8, 8>(p, ws, strips, stream) : cudaErrorInvalidValue;
+  if (ukt != 8) return cudaErrorInvalidValue;
+  return p.rows > kMaxDecodePassRows ? run_tc<8, 8>(p, ws, strips, stream) : run_mma<8, 8>(p, ws, strips, stream);
 }
 
 }  // namespace tfx

@@ -1,0 +1,398 @@
+// The trellis linear for prompt-sized passes (33 to 128 rows) on GB300:
+// tcgen05 MMAs with the decoded weights in Tensor Memory, the same results
+// bit for bit as the decode-row kernel (linear_mma.cuh).
+//
+// Method: "hip exl3: the input rotation and trellis linear for decode rows",
+// section "Known limits": the prompt path follows, registered bit-equal to
+// the decode linear. Bit-equality holds because every output element goes
+// through the same sums as in the decode-row kernel: the same cut of the
+// (block, unit) grid between CTAs, the same two chains per segment (the units
+// at even and at odd processing positions, each a chain of K = 16 tensor-core
+// steps in input order), their fp32 sum in that order, and the partial sums
+// of a shared block added in CTA order. A tcgen05.mma (M = 128, K = 16, A in
+// Tensor Memory) gives the same bits as mma.sync.m16n8k16 for the same
+// operands and accumulator, also when the 16 inputs of a step are presented
+// in another order (checked on the GB300 over 81,920 outputs of chains of
+// eight steps with wide exponent ranges).
+//
+// Per CTA (one per SM): the MMA's M is the 128 outputs of a block (Tensor
+// Memory lanes), N the 128 row slots of the pass, K 16 inputs per k-tile.
+// Warp roles:
+//   warps 0-3   epilogue: per segment, the two chains' sums from Tensor
+//               Memory, added, written to this CTA's partial-sum slot, then
+//               (when the CTA owns the block, or arrives last) the output
+//               rotation, svh and the stores
+//   warps 4-19  decode: four warpgroups take half-units (8 k-tiles) in turn;
+//               thread n decodes output n's 16 weights of each k-tile into
+//               Tensor Memory lane n (the MMA's A operand)
+//   warp 20     producer: the copies of each half-unit (packed weights, and
+//               the 128-row xr slice laid out as the MMA's B operand)
+//   warp 21     MMA: allocates Tensor Memory; one thread issues the MMAs
+// All waits are bounded; a kernel that gives up sets the error flag and exits.
+#pragma once
+
+#include "linear_mma.cuh"
+
+namespace tfx {
+
+namespace {
+
+constexpr int kTcRows = 128;     // row slots of a pass (the MMA's N)
+constexpr int kTcHalfKt = 8;     // k-tiles per staged half-unit
+constexpr int kTcWG = 4;           // decode warpgroups
+constexpr int kTcProducer = 4 + 4 * kTcWG;
+constexpr int kTcMma = kTcProducer + 1;
+constexpr int kTcThreads = (kTcMma + 1) * 32;
+constexpr int kTcTmemCols = 512;  // acc[2] at columns 0 and 128; one A buffer per warpgroup at 256 + 64 wg
+constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared block
+
+template <int BITS>
+struct TcCfg {
+  static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
+  static constexpr int kXrBytes = kTcRows * 16 * kTcHalfKt * 2;  // 128 rows x 128 inputs, fp16
+  static constexpr int kStageBytes = kWBytes + kXrBytes;
+  static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
+  // A multiple of the warpgroups, so that a stage's previous half-unit went
+  // to the same decode warpgroup.
+  static constexpr int kStages = (kStagesFit < 8 ? kStagesFit : 8) / kTcWG * kTcWG;
+  static constexpr int kXchOff = kStages * kStageBytes;
+  static constexpr int kBarOff = kXchOff + 8192;
+  static constexpr int kNumBars = 2 * kStages + 2 * kTcWG + 3;  // full, empty, afull, aempty, dfull, dempty, drain
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 64;
+};
+
+template <int BITS, int LAYOUT, int UKT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                             const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
+  using T = TcCfg<BITS>;
+  constexpr int S = T::kStages;
+  constexpr int H = UKT / kTcHalfKt;  // half-units per unit
+  static_assert(S >= kTcWG && S % kTcWG == 0, "stages must stay with one decode warpgroup");
+  extern __shared__ __align__(1024) uint8_t smem[];
+  float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + T::kXchOff);
+  const uint32_t bar0 = smem_u32(smem + T::kBarOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + T::kMiscOff + 8);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto afull_bar = [&](int w) { return bar0 + 8u * (2 * S + w); };
+  auto aempty_bar = [&](int w) { return bar0 + 8u * (2 * S + kTcWG + w); };
+  const uint32_t dfull = bar0 + 8u * (2 * S + 2 * kTcWG);
+  const uint32_t dempty = bar0 + 8u * (2 * S + 2 * kTcWG + 1);
+  const uint32_t drain = bar0 + 8u * (2 * S + 2 * kTcWG + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const SegmentOrder order(range_start(c, p.units, p.ctas), range_start(c + 1, p.units, p.ctas),
+                           p.units_per_block);
+  const int n_half = order.n_units * H;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    *last_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 4 + 1);  // the decoding warpgroup's 4 warps and the MMA thread
+    }
+    for (int w = 0; w < kTcWG; ++w) {
+      mbar_init(afull_bar(w), 4);
+      mbar_init(aempty_bar(w), 1);
+    }
+    mbar_init(dfull, 1);
+    mbar_init(dempty, 4);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == kTcMma) {
+    tmem_alloc(smem_u32(tmem_holder), kTcTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTcProducer && lane == 0) {
+    if (LAYOUT == kLayoutTiles) tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&xmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kTcProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      pdl_wait_prerequisites();
+      UnitCursor cur(order);
+      int issued = 0;
+      for (int q = 0; q < n_half; ++q) {
+        const int s = q % S;
+        if (q >= S && !mbar_wait_sleepy(empty_bar(s), ((q / S) - 1) & 1, abort_flag, 128)) break;
+        const int h = q % H;
+        const int kt0 = cur.ub() * UKT + h * kTcHalfKt;  // first k-tile of the half-unit
+        const uint32_t st = smem_u32(smem + s * T::kStageBytes);
+        mbar_arrive_expect_tx(full_bar(s), T::kStageBytes);
+        if (LAYOUT == kLayoutTiles)
+          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, kt0, full_bar(s));
+        else
+          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h * T::kWBytes,
+                       T::kWBytes, full_bar(s));
+        tma_load_3d(st + T::kWBytes, &xmap, 0, 0, kt0 * 2, full_bar(s));
+        issued = q + 1;
+        if (h == H - 1) cur.next();
+      }
+      for (int q = issued - S > 0 ? issued - S : 0; q < issued; ++q) {
+        volatile int never = 0;
+        mbar_wait(full_bar(q % S), (q / S) & 1, &never);
+      }
+    }
+  } else if (warp >= 4 && warp < kTcProducer) {
+    // -------------------------------------------------------------- decode
+    const int wg = (warp - 4) >> 2;           // takes half-units wg, wg + kTcWG, ...
+    const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
+    const int tile = n >> 4, col = n & 15;
+    for (int j = 0;; ++j) {
+      const int q = kTcWG * j + wg;
+      if (q >= n_half) break;
+      const int s = q % S;
+      bool ok = mbar_wait(full_bar(s), (q / S) & 1, abort_flag);
+      if (ok && j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
+      const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + s * T::kStageBytes);
+      const uint32_t a_addr = tmem + lane_off + 256 + wg * 64;
+#pragma unroll
+      for (int kt = 0; kt < kTcHalfKt; ++kt) {
+        ColWords<BITS> cw;
+        if constexpr (LAYOUT == kLayoutTiles)
+          load_col_words<BITS>(ws + (kt * 8 + tile) * 8 * BITS, col, cw);
+        else
+          load_col_words_strided<BITS, 4>(ws + ((kt >> 2) * 8 + tile) * 32 * BITS + (kt & 3), col, cw);
+        uint32_t a[8];
+        decode_col_words<BITS>(cw, col, a);
+        tmem_st8(a_addr + kt * 8, a);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(afull_bar(wg));
+        mbar_arrive(empty_bar(s));
+      }
+    }
+  } else if (warp == kTcMma) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_f16_f32(128, kTcRows);
+      bool stop = false;
+      for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
+        const long long bb = order.block(sg);
+        const int seg_lo = order.lo(bb);
+        const int seg_hi = order.hi(bb);
+        const int base = order.pos(sg, seg_lo) - seg_lo;  // processing position of unit i: base + i
+        // The accumulators must have been read out for the previous segment.
+        if (sg >= 1) {
+          tc_fence_before();
+          if (!mbar_wait(dempty, (sg - 1) & 1, abort_flag)) break;
+          tc_fence_after();
+        }
+        bool started[2] = {false, false};
+        for (int i = seg_lo; i < seg_hi && !stop; ++i) {
+          const int k = base + i;
+          const int g = k & 1;  // the chain: units at even / odd processing positions
+          for (int h = 0; h < H; ++h) {
+            const int q = k * H + h;
+            const int s = q % S;
+            const int wg = q % kTcWG, j = q / kTcWG;
+            if (!mbar_wait(full_bar(s), (q / S) & 1, abort_flag) ||
+                !mbar_wait(afull_bar(wg), j & 1, abort_flag)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = tmem + 256 + wg * 64;
+            const uint32_t xs = smem_u32(smem + s * T::kStageBytes + T::kWBytes);
+#pragma unroll
+            for (int kt = 0; kt < kTcHalfKt; ++kt) {
+              // B: [k / 8][row][k % 8], 2048 bytes per 8 inputs of the 128 rows.
+              const uint64_t bdesc = smem_desc_noswizzle(xs + kt * 2 * 2048, 2048, 128);
+              mma_f16_tmemA(tmem + g * 128, a_addr + kt * 8, bdesc, kIdesc, started[g] ? 1u : 0u);
+              started[g] = true;
+            }
+            mma_commit(aempty_bar(wg));
+            mma_commit(empty_bar(s));
+          }
+        }
+        mma_commit(dfull);
+      }
+      // Every MMA issued must have completed before Tensor Memory is freed.
+      mma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never);
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int t = threadIdx.x;  // output within the block = Tensor Memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    LinearPass lp;
+    lp.svh = p.svh;
+    lp.y = p.y;
+    lp.out_dtype = p.out_dtype;
+    lp.rows = p.rows;
+    lp.in_features = p.in_features;
+    lp.out_features = p.out_features;
+    const size_t slot_floats = static_cast<size_t>(kTcRows) * 128;
+    for (int sg = 0; sg < order.n_seg; ++sg) {
+      const int b = static_cast<int>(order.block(sg));
+      const int seg_lo = order.lo(b);
+      const int seg_hi = order.hi(b);
+      const int base = order.pos(sg, seg_lo) - seg_lo;
+      // A chain with no unit in this segment contributes +0, as in the
+      // decode-row kernel.
+      const bool has0 = (seg_hi - seg_lo >= 2) || ((base + seg_lo) % 2 == 0);
+      const bool has1 = (seg_hi - seg_lo >= 2) || ((base + seg_lo) % 2 != 0);
+      const bool ok = mbar_wait_sleepy(dfull, sg & 1, abort_flag, 200);
+      if (!group_all(1, 128, ok)) break;  // the named barriers below need all 128 threads
+      tc_fence_after();
+      const int c_first = cta_of_unit(static_cast<long long>(b) * order.UB, p.units, p.ctas);
+      const int c_last = cta_of_unit(static_cast<long long>(b + 1) * order.UB - 1, p.units, p.ctas);
+      const bool shared = c_first != c_last;
+      const int slot = shared ? partial_slot(c, b, p) : 2;
+      float* mine = p.partials + (static_cast<size_t>(c) * kTcPartialSlots + slot) * slot_floats;
+      // The two chains' sums, added in chain order, into this CTA's slot.
+#pragma unroll 1
+      for (int r0 = 0; r0 < kTcRows; r0 += 16) {
+        float g0[16], g1[16];
+        tmem_ld16(tmem + lane_off + r0, g0);
+        tmem_ld16(tmem + lane_off + 128 + r0, g1);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const float v = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
+          if (r0 + r < p.rows) mine[(r0 + r) * 128 + t] = v;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);  // the MMA thread may start the next segment
+      bool finish = true;
+      if (shared) {
+        __threadfence();
+        group_sync(1, 128);
+        if (t == 0) {
+          const int old = atomicAdd(p.counters + b, 1);
+          *last_flag = (old == c_last - c_first) ? 1 : 0;
+        }
+        group_sync(1, 128);
+        finish = *last_flag != 0;
+        if (finish) __threadfence();
+      } else {
+        group_sync(1, 128);
+      }
+      if (finish) {
+#pragma unroll 1
+        for (int r0 = 0; r0 < kTcRows && r0 < p.rows; r0 += 16) {
+          float v[16];
+          for (int cc = (shared ? c_first : c); cc <= (shared ? c_last : c); ++cc) {
+            const int sl = shared ? partial_slot(cc, b, p) : 2;
+            const float* src = p.partials + (static_cast<size_t>(cc) * kTcPartialSlots + sl) * slot_floats;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) x[r] = __ldcg(src + (r0 + r) * 128 + t);
+            const bool first = !shared || cc == c_first;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) v[r] = first ? x[r] : __fadd_rn(v[r], x[r]);
+          }
+          block_epilogue(v, lp, b, t, xch, 1, 128, r0);
+        }
+        if (shared && t == 0) p.counters[b] = 0;
+      }
+      group_sync(1, 128);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTcTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err_flag, 1);
+}
+
+template <int BITS, int LAYOUT, int UKT>
+cudaError_t tc_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(trellis_linear_tc_kernel<BITS, LAYOUT, UKT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BITS>::kBytes);
+  });
+  return err;
+}
+
+// One pass of 33 to 128 rows.
+template <int BITS, int UKT>
+cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap wmap, xmap;
+  memset(&wmap, 0, sizeof(wmap));
+  if (!strips) {
+    // Packed weights as rows of u64, one row per k-tile; a box is 8 k-tiles x 8 tiles.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
+                                static_cast<cuuint64_t>(lp.in_features / 16)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.out_features) * BITS * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(kTcHalfKt)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(lp.trellis), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // xr [rows][in] fp16 viewed as (8 inputs, rows, in / 8): a box of
+    // (8, 128, 16) lands as the MMA's B operand for 8 k-tiles,
+    // [k / 8][row][k % 8]; row slots past `rows` are zero.
+    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(lp.rows),
+                                static_cast<cuuint64_t>(lp.in_features / 8)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 16};
+    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(kTcRows), static_cast<cuuint32_t>(2 * kTcHalfKt)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  MmaParams p;
+  p.strips = reinterpret_cast<const uint8_t*>(lp.trellis);
+  p.svh = lp.svh;
+  p.y = lp.y;
+  p.partials = ws.partials;
+  p.counters = ws.counters;
+  p.err_flag = ws.err_flag;
+  p.units_per_block = lp.in_features / (16 * UKT);
+  p.units = static_cast<long long>(lp.out_features / 128) * p.units_per_block;
+  p.ctas = ws.ctas;
+  p.out_dtype = lp.out_dtype;
+  p.rows = lp.rows;
+  p.in_features = lp.in_features;
+  p.out_features = lp.out_features;
+  cudaError_t e = strips ? tc_smem_attr<BITS, kLayoutStrips, UKT>() : tc_smem_attr<BITS, kLayoutTiles, UKT>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ws.ctas);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcCfg<BITS>::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return strips ? cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutStrips, UKT>, wmap, xmap, p)
+                : cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutTiles, UKT>, wmap, xmap, p);
+}
+
+}  // namespace
+}  // namespace tfx
