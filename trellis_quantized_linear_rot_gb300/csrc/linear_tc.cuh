@@ -26,7 +26,9 @@
 //               thread n decodes output n's 16 weights of each k-tile into
 //               Tensor Memory lane n (the MMA's A operand)
 //   warp 20     producer: the copies of each half-unit (packed weights, and
-//               the 128-row xr slice laid out as the MMA's B operand)
+//               the xr slice of the pass's row slots: two tensor copies of
+//               64 inputs x N rows with the 128-byte swizzle, which is the
+//               MMA's K-major B layout)
 //   warp 21     MMA: allocates Tensor Memory; one thread issues the MMAs
 // All waits are bounded; a kernel that gives up sets the error flag and exits.
 #pragma once
@@ -49,7 +51,7 @@ constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared bloc
 template <int BITS>
 struct TcCfg {
   static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
-  static constexpr int kXrBytes = kTcRows * 16 * kTcHalfKt * 2;  // 128 rows x 128 inputs, fp16
+  static constexpr int kXrBytes = kTcRows * 16 * kTcHalfKt * 2;  // up to 128 rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
@@ -61,6 +63,10 @@ struct TcCfg {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
 };
+
+// The pass's row slots: `rows` rounded up to 16 (the MMA's N); slots past
+// `rows` read zeros.
+__host__ __device__ constexpr int tc_row_slots(int rows) { return (rows + 15) & ~15; }
 
 template <int BITS, int LAYOUT, int UKT>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -90,9 +96,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const SegmentOrder order(range_start(c, p.units, p.ctas), range_start(c + 1, p.units, p.ctas),
                            p.units_per_block);
   const int n_half = order.n_units * H;
+  const int nslots = tc_row_slots(p.rows);
+  const uint32_t xr_box_bytes = static_cast<uint32_t>(nslots) * 128;  // 64 inputs x nslots rows
 
   if (threadIdx.x == 0) {
-    *abort_flag = 0;
+    // The swizzled B tiles need 1024-byte alignment (their offsets in a stage
+    // are multiples of 1024).
+    *abort_flag = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
     *last_flag = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -132,13 +142,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int h = q % H;
         const int kt0 = cur.ub() * UKT + h * kTcHalfKt;  // first k-tile of the half-unit
         const uint32_t st = smem_u32(smem + s * T::kStageBytes);
-        mbar_arrive_expect_tx(full_bar(s), T::kStageBytes);
+        mbar_arrive_expect_tx(full_bar(s), T::kWBytes + 2 * xr_box_bytes);
         if (LAYOUT == kLayoutTiles)
           tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, kt0, full_bar(s));
         else
           bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h * T::kWBytes,
                        T::kWBytes, full_bar(s));
-        tma_load_3d(st + T::kWBytes, &xmap, 0, 0, kt0 * 2, full_bar(s));
+        tma_load_2d(st + T::kWBytes, &xmap, kt0 * 16, 0, full_bar(s));
+        tma_load_2d(st + T::kWBytes + xr_box_bytes, &xmap, kt0 * 16 + 64, 0, full_bar(s));
         issued = q + 1;
         if (h == H - 1) cur.next();
       }
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kTcMma) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_f16_f32(128, kTcRows);
+      const uint32_t idesc = idesc_f16_f32(128, nslots);
       bool stop = false;
       for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
         const long long bb = order.block(sg);
@@ -215,9 +226,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t xs = smem_u32(smem + s * T::kStageBytes + T::kWBytes);
 #pragma unroll
             for (int kt = 0; kt < kTcHalfKt; ++kt) {
-              // B: [k / 8][row][k % 8], 2048 bytes per 8 inputs of the 128 rows.
-              const uint64_t bdesc = smem_desc_noswizzle(xs + kt * 2 * 2048, 2048, 128);
-              mma_f16_tmemA(tmem + g * 128, a_addr + kt * 8, bdesc, kIdesc, started[g] ? 1u : 0u);
+              // B: k-tile kt is inputs 16 (kt % 4) .. + 15 of the swizzled
+              // tile kt / 4 (rows of 128 bytes, 8-row groups 1024 apart).
+              const uint64_t bdesc = smem_desc_sw128(xs + (kt >> 2) * xr_box_bytes + (kt & 3) * 32, 1024);
+              mma_f16_tmemA(tmem + g * 128, a_addr + kt * 8, bdesc, idesc, started[g] ? 1u : 0u);
               started[g] = true;
             }
             mma_commit(aempty_bar(wg));
@@ -262,15 +274,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float* mine = p.partials + (static_cast<size_t>(c) * kTcPartialSlots + slot) * slot_floats;
       // The two chains' sums, added in chain order, into this CTA's slot.
 #pragma unroll 1
-      for (int r0 = 0; r0 < kTcRows; r0 += 16) {
+      for (int r0 = 0; r0 < p.rows; r0 += 16) {
         float g0[16], g1[16];
         tmem_ld16(tmem + lane_off + r0, g0);
         tmem_ld16(tmem + lane_off + 128 + r0, g1);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          const float v = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
-          if (r0 + r < p.rows) mine[(r0 + r) * 128 + t] = v;
-        }
+        for (int r = 0; r < 16; ++r) mine[(r0 + r) * 128 + t] = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
       }
       tc_fence_before();
       __syncwarp();
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (finish) {
 #pragma unroll 1
-        for (int r0 = 0; r0 < kTcRows && r0 < p.rows; r0 += 16) {
+        for (int r0 = 0; r0 < p.rows; r0 += 16) {
           float v[16];
           for (int cc = (shared ? c_first : c); cc <= (shared ? c_last : c); ++cc) {
             const int sl = shared ? partial_slot(cc, b, p) : 2;
@@ -303,7 +312,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int r = 0; r < 16; ++r) v[r] = first ? x[r] : __fadd_rn(v[r], x[r]);
           }
-          block_epilogue(v, lp, b, t, xch, 1, 128, r0);
+          // All 16 slots go through the rotation (the ones past `rows` hold
+          // zeros): straight-line code, no per-row predicates.
+          fwht_outputs(v, 16, t, xch, 1, 128);
+          store_outputs(v, lp, b, t, r0);
         }
         if (shared && t == 0) p.counters[b] = 0;
       }
@@ -351,16 +363,15 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
       return cudaErrorInvalidValue;
   }
   {
-    // xr [rows][in] fp16 viewed as (8 inputs, rows, in / 8): a box of
-    // (8, 128, 16) lands as the MMA's B operand for 8 k-tiles,
-    // [k / 8][row][k % 8]; row slots past `rows` are zero.
-    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(lp.rows),
-                                static_cast<cuuint64_t>(lp.in_features / 8)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 16};
-    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(kTcRows), static_cast<cuuint32_t>(2 * kTcHalfKt)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    // xr [rows][in] fp16; a box is 64 inputs (128 bytes) x the pass's row
+    // slots, written with the 128-byte swizzle: the MMA's K-major B operand
+    // for 4 k-tiles. Slots past `rows` are filled with zeros.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.in_features), static_cast<cuuint64_t>(lp.rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.in_features) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(tc_row_slots(lp.rows))};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(lp.xr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

@@ -191,6 +191,23 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
   return d;
 }
 
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of
+// 64 16-bit elements (128 bytes) at a 128-byte pitch, their 16-byte chunks
+// permuted by XOR with row % 8 (the order a tensor copy with the 128-byte
+// swizzle writes); `sbo` = byte distance between 8-row groups. The layout
+// needs no leading offset (the field holds 16 bytes). The atom (8 rows) must
+// sit on a 1024-byte boundary; a K step inside it adds 32 bytes per 16
+// elements to the start address. Bits 61-63 = 2 select this swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.
 __device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
