@@ -194,55 +194,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == kTcMma) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(128, nslots);
-      bool stop = false;
-      for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
-        const long long bb = order.block(sg);
-        const int seg_lo = order.lo(bb);
-        const int seg_hi = order.hi(bb);
-        const int base = order.pos(sg, seg_lo) - seg_lo;  // processing position of unit i: base + i
-        // The accumulators must have been read out for the previous segment.
-        if (sg >= 1) {
-          tc_fence_before();
-          if (!mbar_wait(dempty, (sg - 1) & 1, abort_flag)) break;
+    // The whole warp runs the loop and one elected lane issues, so that the
+    // operands stay in uniform registers: issued from a lone lane, each MMA
+    // costs more than its tensor-core time at these sizes.
+    const uint32_t idesc = idesc_f16_f32(128, nslots);
+    // B descriptors: the first stage's xr slice, advanced in 16-byte units.
+    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + T::kWBytes), 1024);
+    const uint32_t box_step = xr_box_bytes >> 4;
+    const uint32_t stage_step = static_cast<uint32_t>(T::kStageBytes) >> 4;
+    bool stop = false;
+    for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
+      const long long bb = order.block(sg);
+      const int seg_lo = order.lo(bb);
+      const int seg_hi = order.hi(bb);
+      const int base = order.pos(sg, seg_lo) - seg_lo;  // processing position of unit i: base + i
+      // The accumulators must have been read out for the previous segment.
+      if (sg >= 1) {
+        tc_fence_before();
+        if (!__all_sync(0xffffffffu, mbar_wait(dempty, (sg - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+      }
+      uint32_t started = 0;  // bit g: chain g has had its first step
+      for (int i = seg_lo; i < seg_hi && !stop; ++i) {
+        const int k = base + i;
+        const int g = k & 1;  // the chain: units at even / odd processing positions
+        const uint32_t d_addr = tmem + g * 128;
+        for (int h = 0; h < H; ++h) {
+          const int q = k * H + h;
+          const int s = q % S;
+          const int wg = q % kTcWG, j = q / kTcWG;
+          bool ok = mbar_wait(full_bar(s), (q / S) & 1, abort_flag);
+          ok = ok && mbar_wait(afull_bar(wg), j & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            stop = true;
+            break;
+          }
           tc_fence_after();
-        }
-        bool started[2] = {false, false};
-        for (int i = seg_lo; i < seg_hi && !stop; ++i) {
-          const int k = base + i;
-          const int g = k & 1;  // the chain: units at even / odd processing positions
-          for (int h = 0; h < H; ++h) {
-            const int q = k * H + h;
-            const int s = q % S;
-            const int wg = q % kTcWG, j = q / kTcWG;
-            if (!mbar_wait(full_bar(s), (q / S) & 1, abort_flag) ||
-                !mbar_wait(afull_bar(wg), j & 1, abort_flag)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_addr = tmem + 256 + wg * 64;
-            const uint32_t xs = smem_u32(smem + s * T::kStageBytes + T::kWBytes);
+          const uint32_t a_addr = tmem + 256 + wg * 64;
+          const uint64_t bd = bdesc0 + s * stage_step;
+          const uint32_t acc0 = (started >> g) & 1u;
+          if (elect_one()) {
 #pragma unroll
             for (int kt = 0; kt < kTcHalfKt; ++kt) {
               // B: k-tile kt is inputs 16 (kt % 4) .. + 15 of the swizzled
               // tile kt / 4 (rows of 128 bytes, 8-row groups 1024 apart).
-              const uint64_t bdesc = smem_desc_sw128(xs + (kt >> 2) * xr_box_bytes + (kt & 3) * 32, 1024);
-              mma_f16_tmemA(tmem + g * 128, a_addr + kt * 8, bdesc, idesc, started[g] ? 1u : 0u);
-              started[g] = true;
+              mma_f16_tmemA(d_addr, a_addr + kt * 8, bd + (kt >> 2) * box_step + (kt & 3) * 2, idesc,
+                            kt > 0 ? 1u : acc0);
             }
             mma_commit(aempty_bar(wg));
             mma_commit(empty_bar(s));
           }
+          __syncwarp();
+          started |= 1u << g;
         }
-        mma_commit(dfull);
       }
-      // Every MMA issued must have completed before Tensor Memory is freed.
-      mma_commit(drain);
-      volatile int never = 0;
-      mbar_wait(drain, 0, &never);
+      if (elect_one()) mma_commit(dfull);
+      __syncwarp();
     }
+    // Every MMA issued must have completed before Tensor Memory is freed.
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(drain, 0, &never);
   } else {
     // ----------------------------------------------------------- epilogue
     const int t = threadIdx.x;  // output within the block = Tensor Memory lane

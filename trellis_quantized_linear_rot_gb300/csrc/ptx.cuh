@@ -219,6 +219,19 @@ __device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// True in one lane of the warp (all 32 lanes must execute it): the issuer of
+// single-thread instructions inside code the whole warp runs, so that the
+// operands stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 R;\n\t"
+      "elect.sync R|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrive once on `bar` when every MMA this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
