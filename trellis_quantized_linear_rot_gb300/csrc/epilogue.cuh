@@ -9,7 +9,8 @@
 //
 // Thread n (0..127) of a 128-thread group holds output n of the block for the
 // 16 row slots; stages h = 1..16 are lane shuffles, h = 32 and 64 go through
-// shared memory. Only the first `rows` slots are computed and stored.
+// shared memory. Only the first `rows` slots are stored; the rotation runs on
+// 1, 4, 8 or 16 slots, the next count up from `rows`.
 #pragma once
 
 #include <cstdint>
@@ -32,32 +33,45 @@ __device__ __forceinline__ void group_sync(int bar_id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void fwht_outputs(float (&v)[16], int rows, int n, float (*xch)[128],
-                                             int bar_id = 0, int nthreads = 128) {
+// The rotation of the first R row slots, as straight-line code (no per-row
+// predicates, so the shuffles of different rows overlap).
+template <int R>
+__device__ __forceinline__ void fwht_rows(float (&v)[16], int n, float (*xch)[128], int bar_id, int nthreads) {
   const int lane = n & 31;
 #pragma unroll
   for (int m = 1; m <= 16; m <<= 1) {
     const bool upper = (lane & m) != 0;
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      if (r < rows) {
-        const float q = __shfl_xor_sync(0xffffffffu, v[r], m);
-        v[r] = butterfly(v[r], q, upper);
-      }
+    for (int r = 0; r < R; ++r) {
+      const float q = __shfl_xor_sync(0xffffffffu, v[r], m);
+      v[r] = butterfly(v[r], q, upper);
     }
   }
 #pragma unroll
   for (int m = 32; m <= 64; m <<= 1) {
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < rows) xch[r][n] = v[r];
+    for (int r = 0; r < R; ++r) xch[r][n] = v[r];
     group_sync(bar_id, nthreads);
     const bool upper = (n & m) != 0;
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < rows) v[r] = butterfly(v[r], xch[r][n ^ m], upper);
+    for (int r = 0; r < R; ++r) v[r] = butterfly(v[r], xch[r][n ^ m], upper);
     group_sync(bar_id, nthreads);
   }
+}
+
+// The rotation of the first `rows` (1..16) row slots. It runs on 1, 4, 8 or
+// 16 slots (the next count up); rows are independent, so the extra slots
+// change nothing in the ones that are stored.
+__device__ __forceinline__ void fwht_outputs(float (&v)[16], int rows, int n, float (*xch)[128],
+                                             int bar_id = 0, int nthreads = 128) {
+  if (rows > 8)
+    fwht_rows<16>(v, n, xch, bar_id, nthreads);
+  else if (rows > 4)
+    fwht_rows<8>(v, n, xch, bar_id, nthreads);
+  else if (rows > 1)
+    fwht_rows<4>(v, n, xch, bar_id, nthreads);
+  else
+    fwht_rows<1>(v, n, xch, bar_id, nthreads);
 }
 
 // Stores rows row0 .. row0 + 15 of the pass (those below p.rows).
