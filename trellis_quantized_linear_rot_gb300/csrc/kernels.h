@@ -24,11 +24,12 @@ cudaError_t launch_trellis_decode(const uint32_t* trellis, __half* w, int in_fea
 // Rows of one pass of the linear: the weights are decoded once per pass, and
 // each decoded tile feeds the MMAs of all the pass's rows. Passes of up to
 // kMaxDecodePassRows rows run the mma.sync kernel, longer ones (the prompt
-// side) the tcgen05 kernel; both give every row the same bits.
-constexpr int kMaxDecodePassRows = 32;
+// side) the tcgen05 kernel, which is the faster one from 17 rows on; both
+// give every row the same bits.
+constexpr int kMaxDecodePassRows = 16;
 constexpr int kMaxPassRows = 128;
 // Partial sums per CTA the workspace holds: the larger of the two kernels'
-// needs ([2][32][128] and [3][128][128] fp32).
+// needs ([2][16][128] and [3][128][128] fp32).
 constexpr size_t kPartialFloatsPerCta = 3 * 128 * 128;
 
 // One pass of at most kMaxPassRows rows through the trellis linear.

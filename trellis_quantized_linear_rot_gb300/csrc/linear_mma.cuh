@@ -62,13 +62,14 @@ constexpr int kGroups = 2;           // compute groups of 8 warps, alternating u
 constexpr int kComputeWarps = kTileWarps * kGroups;
 constexpr int kThreads = (4 + kComputeWarps + 1) * 32;
 constexpr int kSmemBudget = 196 * 1024;
-constexpr int kSmemBudgetWide = 227 * 1024;  // passes of 32 rows (the per-block maximum)
+constexpr int kSmemBudgetWide = 227 * 1024;  // the per-block maximum (the tcgen05 kernel)
 
-// A pass of up to 8 * NB rows: its MMAs cover NB blocks of 8 row slots, and
-// its sums and xr slices have room for 16 row slots (NB <= 2) or 8 * NB.
+// A pass of up to 8 * NB rows (NB = 1 or 2): its MMAs cover NB blocks of 8
+// row slots; its sums and xr slices have room for 16 row slots.
 template <int NB>
 struct Slots {
-  static constexpr int kRows = NB <= 2 ? 16 : 8 * NB;
+  static_assert(NB == 1 || NB == 2, "passes of up to 16 rows");
+  static constexpr int kRows = 16;
 };
 
 // A unit is UKT k-tiles (16 * UKT inputs) of one output block: 8, or 16 when
@@ -81,8 +82,7 @@ struct Cfg {
   static constexpr int kXrUnitBytes = kXrChunkBytes * (UKT / 4);
   static constexpr int kStageBytes = kWUnitBytes + kXrUnitBytes;
   static constexpr int kDbufBytes = 2 * kGroups * kSlots * 128 * 4;  // [2][groups][slots][128] fp32
-  static constexpr int kBudget = NB <= 2 ? kSmemBudget : kSmemBudgetWide;
-  static constexpr int kStagesFit = (kBudget - kDbufBytes - 8192 - 1024) / kStageBytes;
+  static constexpr int kStagesFit = (kSmemBudget - kDbufBytes - 8192 - 1024) / kStageBytes;
   // Even, so that unit k and unit k - kStages (the stage's previous unit)
   // always belong to the same compute group (see the kernel).
   static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) & ~1;
@@ -237,28 +237,6 @@ __device__ __forceinline__ void strips_unit(const uint4* tq, const uint8_t* xs, 
                                             const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
                                             float (&d)[NB][4]) {
   constexpr int kChunk = 128 * Slots<NB>::kRows;
-  if constexpr (NB > 2) {
-    // Passes of 32 rows hold 16 accumulators per lane: they load one k-tile's
-    // words at a time (32-bit loads from the interleaved chunks) to stay
-    // within the registers.
-#pragma unroll
-    for (int kt = 0; kt < UKT; ++kt) {
-      const uint32_t* tw = reinterpret_cast<const uint32_t*>(tq + (kt >> 2) * 64 * BITS) + (kt & 3);
-      Group4Words<BITS> wa, wb;
-      wa.x[0] = tw[4 * pos_a.w0];
-      wa.x[1] = tw[4 * pos_a.w1];
-      wb.x[0] = tw[4 * pos_b.w0];
-      wb.x[1] = tw[4 * pos_b.w1];
-      if constexpr (Group4<BITS>::kWords == 3) {
-        wa.x[2] = tw[4 * pos_a.w2];
-        wb.x[2] = tw[4 * pos_b.w2];
-      }
-      uint2 b[NB];
-      load_b<NB>(xs + (kt >> 2) * kChunk + xoff[kt & 3], b);
-      tile_step<BITS, NB>(wa, wb, pos_a, pos_b, b, d);
-    }
-    return;
-  }
   Group4Quads<BITS> qa, qb;
   load_group4_quads<BITS>(tq, pos_a, qa);
   load_group4_quads<BITS>(tq, pos_b, qb);
@@ -610,7 +588,6 @@ cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const M
 template <int BITS, int LAYOUT, int UKT>
 cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
                        cudaStream_t stream) {
-  if (p.rows > 16) return launch_one<BITS, 4, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
   if (p.rows > 8) return launch_one<BITS, 2, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
   return launch_one<BITS, 1, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
 }
@@ -641,7 +618,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows),
                                 static_cast<cuuint64_t>(lp.in_features / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};
-    const cuuint32_t box[3] = {64, lp.rows > 16 ? 32u : 16u, static_cast<cuuint32_t>(UKT / 4)};
+    const cuuint32_t box[3] = {64, 16u, static_cast<cuuint32_t>(UKT / 4)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -1,4 +1,4 @@
-// The trellis linear for prompt-sized passes (33 to 128 rows) on GB300:
+// The trellis linear for prompt-sized passes (17 to 128 rows) on GB300:
 // tcgen05 MMAs with the decoded weights in Tensor Memory, the same results
 // bit for bit as the decode-row kernel (linear_mma.cuh).
 //
@@ -356,7 +356,7 @@ cudaError_t tc_smem_attr() {
   return err;
 }
 
-// One pass of 33 to 128 rows.
+// One pass of 17 to 128 rows.
 template <int BITS, int UKT>
 cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   auto encode = encode_fn();
