@@ -96,8 +96,10 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
  *   (fp16 bit patterns; 0x1EEE = 0.00676727294921875, 0xC2E8 = -3.453125).
  * svh:     [out_features] fp16
  * y:       [rows][out_features], out_dtype TF_F16, TF_F32 or TF_BF16, written
- * rows >= 0 (0 launches nothing). Rows run in passes of up to 128 (up to 16
- * on the decode-row kernel, 17 to 128 on the tcgen05 kernel), each pass
+ * rows >= 0 (0 launches nothing). Rows run in passes of up to 128 on one of
+ * two kernels (an mma.sync kernel for passes of up to 8 rows at 2 to 5 bits
+ * in the strips order, a tcgen05 kernel otherwise; the choice changes no
+ * bit), each pass
  * decoding the weights once for all its rows ("Known limits": the prompt
  * path, registered bit-equal to this linear): a row's outputs are the same
  * bits whatever pass, slot or batch it runs in, alone or among up to 128

@@ -213,6 +213,7 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
   ws.counters = ctx->counters;
   ws.err_flag = ctx->err_flag;
   ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
+  ws.partial_floats_per_cta = kPartialFloatsPerCta;
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
   for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
     LinearPass p;
@@ -283,6 +284,7 @@ tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* 
   if (s != TF_OK) return s;
   TcWorkspace ws;
   ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
+  ws.partial_floats_per_cta = kPartialFloatsPerCta;
   const size_t part = ws_partial_bytes(ws.ctas);
   if (workspace_bytes < part + static_cast<size_t>(out_features / 128) * sizeof(int)) return TF_ERR_SCRATCH;
   ws.partials = static_cast<float*>(workspace);

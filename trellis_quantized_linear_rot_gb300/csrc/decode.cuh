@@ -279,6 +279,42 @@ __device__ __forceinline__ void quads_to_words(const Group4Quads<BITS>& gq, Grou
   for (int i = 0; i < Group4<BITS>::kWords; ++i) gw.x[i] = quad_word<KK>(gq.q[i]);
 }
 
+// Column form over the strips order: the words column n needs for four
+// consecutive k-tiles (word w of k-tile kk at 4w + kk), one 128-bit load per
+// word, then k-tile KK's words out of them.
+template <int BITS>
+struct ColQuads {
+  uint4 q[ColWords<BITS>::kCount];
+};
+
+template <int BITS>
+__device__ __forceinline__ void load_col_quads(const uint4* tq, int n, ColQuads<BITS>& cq) {
+  if constexpr (BITS == 4) {
+    cq.q[0] = tq[(2 * n + 31) & 31];
+    cq.q[1] = tq[2 * n];
+    cq.q[2] = tq[2 * n + 1];
+  } else if constexpr (BITS == 8) {
+    cq.q[0] = tq[(4 * n + 63) & 63];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cq.q[1 + j] = tq[4 * n + j];
+  } else {
+    using S = RowSpan<BITS>;
+    const int w0 = row_first_bit<BITS>(n) >> 5;
+#pragma unroll
+    for (int j = 0; j < S::kWords; ++j) {
+      int wi = w0 + j;
+      wi = (wi >= S::kTileWords) ? wi - S::kTileWords : wi;
+      cq.q[j] = tq[wi];
+    }
+  }
+}
+
+template <int BITS, int KK>
+__device__ __forceinline__ void quads_to_col_words(const ColQuads<BITS>& cq, ColWords<BITS>& cw) {
+#pragma unroll
+  for (int i = 0; i < ColWords<BITS>::kCount; ++i) cw.w[i] = quad_word<KK>(cq.q[i]);
+}
+
 // The arithmetic: packs weights (4t, 4t+1) and (4t+2, 4t+3) as two half2 words.
 template <int BITS>
 __device__ __forceinline__ void decode_group4_words(const Group4Words<BITS>& gw, int off, uint32_t& lo,

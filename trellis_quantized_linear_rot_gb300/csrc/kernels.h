@@ -22,15 +22,27 @@ cudaError_t launch_trellis_decode(const uint32_t* trellis, __half* w, int in_fea
                                   int out_features, int bits, cudaStream_t stream);
 
 // Rows of one pass of the linear: the weights are decoded once per pass, and
-// each decoded tile feeds the MMAs of all the pass's rows. Passes of up to
-// kMaxDecodePassRows rows run the mma.sync kernel, longer ones (the prompt
-// side) the tcgen05 kernel, which is the faster one from 17 rows on; both
-// give every row the same bits.
+// each decoded tile feeds the MMAs of all the pass's rows. Two kernels give
+// every row the same bits: the mma.sync kernel (passes of up to
+// kMaxDecodePassRows rows) and the tcgen05 kernel (up to kMaxPassRows).
 constexpr int kMaxDecodePassRows = 16;
 constexpr int kMaxPassRows = 128;
-// Partial sums per CTA the workspace holds: the larger of the two kernels'
-// needs ([2][16][128] and [3][128][128] fp32).
-constexpr size_t kPartialFloatsPerCta = 3 * 128 * 128;
+// Partial sums per CTA: the tcgen05 kernel's [3][128][128] and the mma.sync
+// kernel's [2][16][128] fp32. The library's workspaces hold the larger.
+constexpr size_t kTcPartialFloatsPerCta = 3 * 128 * 128;
+constexpr size_t kMmaPartialFloatsPerCta = 2 * 16 * 128;
+constexpr size_t kPartialFloatsPerCta = kTcPartialFloatsPerCta;
+
+// The kernel of a pass, as measured on the GB300 (LM head and wkv shapes):
+// the mma.sync kernel is faster for passes of up to 8 rows at 2 to 5 bits in
+// the strips order; the tcgen05 kernel everywhere else (up to 18 % at 6 and
+// 8 bits, and in the k-tile order). A workspace too small for the tcgen05
+// kernel's partial sums keeps passes of up to 16 rows on the mma.sync one.
+inline bool pass_uses_tc(int rows, int bits, bool strips, size_t partial_floats_per_cta) {
+  if (rows > kMaxDecodePassRows) return true;
+  if (partial_floats_per_cta < kTcPartialFloatsPerCta) return false;
+  return !(strips && bits <= 5 && rows <= 8);
+}
 
 // One pass of at most kMaxPassRows rows through the trellis linear.
 struct LinearPass {
@@ -61,10 +73,11 @@ struct DeviceCtx {
 // between CTAs ([ctas][2][16][128] fp32) and one arrival counter per output
 // block (zero between calls).
 struct TcWorkspace {
-  float* partials;
+  float* partials;                // partial sums: room for partial_floats_per_cta fp32 per CTA
   int* counters;
   int* err_flag;
   int ctas;
+  size_t partial_floats_per_cta;  // capacity per CTA (picks the kernels it can serve)
 };
 
 int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features, int bits);

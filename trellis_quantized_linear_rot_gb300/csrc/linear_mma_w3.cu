@@ -6,8 +6,9 @@ namespace tfx {
 
 cudaError_t run_trellis_linear_w3(const LinearPass& p, const TcWorkspace& ws, bool strips, int ukt,
                                   cudaStream_t stream) {
-  if (p.rows > kMaxDecodePassRows)
+  if (pass_uses_tc(p.rows, 3, strips, ws.partial_floats_per_cta))
     return ukt == 16 ? run_tc<3, 16>(p, ws, strips, stream) : run_tc<3, 8>(p, ws, strips, stream);
+  if (p.rows > kMaxDecodePassRows) return cudaErrorInvalidValue;
   return ukt == 16 ? run_mma<3, 16>(p, ws, strips, stream) : run_mma<3, 8>(p, ws, strips, stream);
 }
 

@@ -8,7 +8,9 @@ cudaError_t run_trellis_linear_w8(const LinearPass& p, const TcWorkspace& ws, bo
                                   cudaStream_t stream) {
   // Units of 8 k-tiles at this width (16 only up to 5 bits).
   if (ukt != 8) return cudaErrorInvalidValue;
-  return p.rows > kMaxDecodePassRows ? run_tc<8, 8>(p, ws, strips, stream) : run_mma<8, 8>(p, ws, strips, stream);
+  if (pass_uses_tc(p.rows, 8, strips, ws.partial_floats_per_cta)) return run_tc<8, 8>(p, ws, strips, stream);
+  if (p.rows > kMaxDecodePassRows) return cudaErrorInvalidValue;
+  return run_mma<8, 8>(p, ws, strips, stream);
 }
 
 }  // namespace tfx

@@ -86,6 +86,7 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
   ws.partials = reinterpret_cast<float*>(scratch);
   ws.counters = reinterpret_cast<int*>(scratch + kPartialFloats * sizeof(float));
   ws.err_flag = err_flag;
+  ws.partial_floats_per_cta = kMmaPartialFloatsPerCta;  // passes of 16 rows, mma.sync kernel only
   ws.ctas = trellis_linear_mma_ctas(num_sms < kNoAllocMaxCtas ? num_sms : kNoAllocMaxCtas, in_features,
                                     out_features, bits);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -16,7 +16,8 @@
 // eight steps with wide exponent ranges).
 //
 // Per CTA (one per SM): the MMA's M is the 128 outputs of a block (Tensor
-// Memory lanes), N the 128 row slots of the pass, K 16 inputs per k-tile.
+// Memory lanes), N the pass's row slots (rows rounded up to 16, at most 128),
+// K 16 inputs per k-tile.
 // Warp roles:
 //   warps 0-3   epilogue: per segment, the two chains' sums from Tensor
 //               Memory, added, written to this CTA's partial-sum slot, then
@@ -25,11 +26,13 @@
 //   warps 4-19  decode: four warpgroups take half-units (8 k-tiles) in turn;
 //               thread n decodes output n's 16 weights of each k-tile into
 //               Tensor Memory lane n (the MMA's A operand)
-//   warp 20     producer: the copies of each half-unit (packed weights, and
+//   warp 20     producer: the copies of each half-unit into a ring of
+//               stages sized by the pass's row-slot class (packed weights, and
 //               the xr slice of the pass's row slots: two tensor copies of
 //               64 inputs x N rows with the 128-byte swizzle, which is the
 //               MMA's K-major B layout)
-//   warp 21     MMA: allocates Tensor Memory; one thread issues the MMAs
+//   warp 21     MMA: allocates Tensor Memory; the warp runs the MMA loop and
+//               one elected lane issues
 // All waits are bounded; a kernel that gives up sets the error flag and exits.
 #pragma once
 
@@ -48,15 +51,20 @@ constexpr int kTcThreads = (kTcMma + 1) * 32;
 constexpr int kTcTmemCols = 512;  // acc[2] at columns 0 and 128; one A buffer per warpgroup at 256 + 64 wg
 constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared block
 
-template <int BITS>
+// Shared memory of a pass class: stages of a half-unit's packed weights and
+// its xr slice for up to SLOTS row slots (32, 64 or 128). Fewer slots make
+// smaller stages and so more of them in flight: 12 / 8 / 4 at 4 bits (the
+// copies of a stage take longer to land than a warpgroup takes to decode
+// one half-unit, so a warpgroup needs stages beyond the one it decodes).
+template <int BITS, int SLOTS>
 struct TcCfg {
   static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
-  static constexpr int kXrBytes = kTcRows * 16 * kTcHalfKt * 2;  // up to 128 rows x 128 inputs, fp16
+  static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // up to SLOTS rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
   // to the same decode warpgroup.
-  static constexpr int kStages = (kStagesFit < 8 ? kStagesFit : 8) / kTcWG * kTcWG;
+  static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) / kTcWG * kTcWG;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
   static constexpr int kNumBars = 2 * kStages + 2 * kTcWG + 3;  // full, empty, afull, aempty, dfull, dempty, drain
@@ -64,15 +72,25 @@ struct TcCfg {
   static constexpr int kBytes = kMiscOff + 64;
 };
 
+// Decodes k-tile KK of four (strips order) into Tensor Memory at `a_addr`.
+template <int BITS, int KK>
+__device__ __forceinline__ void tc_decode_kt(const ColQuads<BITS>& cq, int col, uint32_t a_addr) {
+  ColWords<BITS> cw;
+  quads_to_col_words<BITS, KK>(cq, cw);
+  uint32_t a[8];
+  decode_col_words<BITS>(cw, col, a);
+  tmem_st8(a_addr, a);
+}
+
 // The pass's row slots: `rows` rounded up to 16 (the MMA's N); slots past
 // `rows` read zeros.
 __host__ __device__ constexpr int tc_row_slots(int rows) { return (rows + 15) & ~15; }
 
-template <int BITS, int LAYOUT, int UKT>
+template <int BITS, int LAYOUT, int UKT, int SLOTS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                              const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
-  using T = TcCfg<BITS>;
+  using T = TcCfg<BITS, SLOTS>;
   constexpr int S = T::kStages;
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
   static_assert(S >= kTcWG && S % kTcWG == 0, "stages must stay with one decode warpgroup");
@@ -173,16 +191,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
       const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + s * T::kStageBytes);
       const uint32_t a_addr = tmem + lane_off + 256 + wg * 64;
+      if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
-      for (int kt = 0; kt < kTcHalfKt; ++kt) {
-        ColWords<BITS> cw;
-        if constexpr (LAYOUT == kLayoutTiles)
+        for (int kt = 0; kt < kTcHalfKt; ++kt) {
+          ColWords<BITS> cw;
           load_col_words<BITS>(ws + (kt * 8 + tile) * 8 * BITS, col, cw);
-        else
-          load_col_words_strided<BITS, 4>(ws + ((kt >> 2) * 8 + tile) * 32 * BITS + (kt & 3), col, cw);
-        uint32_t a[8];
-        decode_col_words<BITS>(cw, col, a);
-        tmem_st8(a_addr + kt * 8, a);
+          uint32_t a[8];
+          decode_col_words<BITS>(cw, col, a);
+          tmem_st8(a_addr + kt * 8, a);
+        }
+      } else {
+        // Strips: one 128-bit load per word brings it for four k-tiles.
+#pragma unroll
+        for (int c4 = 0; c4 < kTcHalfKt / 4; ++c4) {
+          ColQuads<BITS> cq;
+          load_col_quads<BITS>(reinterpret_cast<const uint4*>(ws + (c4 * 8 + tile) * 32 * BITS), col, cq);
+          tc_decode_kt<BITS, 0>(cq, col, a_addr + (4 * c4 + 0) * 8);
+          tc_decode_kt<BITS, 1>(cq, col, a_addr + (4 * c4 + 1) * 8);
+          tc_decode_kt<BITS, 2>(cq, col, a_addr + (4 * c4 + 2) * 8);
+          tc_decode_kt<BITS, 3>(cq, col, a_addr + (4 * c4 + 3) * 8);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -345,15 +373,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.err_flag, 1);
 }
 
-template <int BITS, int LAYOUT, int UKT>
+template <int BITS, int LAYOUT, int UKT, int SLOTS>
 cudaError_t tc_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(trellis_linear_tc_kernel<BITS, LAYOUT, UKT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BITS>::kBytes);
+    err = cudaFuncSetAttribute(trellis_linear_tc_kernel<BITS, LAYOUT, UKT, SLOTS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BITS, SLOTS>::kBytes);
   });
   return err;
+}
+
+// Launches the kernel of row-slot class SLOTS.
+template <int BITS, int UKT, int SLOTS>
+cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, bool strips, int ctas,
+                      cudaStream_t stream) {
+  cudaError_t e = strips ? tc_smem_attr<BITS, kLayoutStrips, UKT, SLOTS>() : tc_smem_attr<BITS, kLayoutTiles, UKT, SLOTS>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcCfg<BITS, SLOTS>::kBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return strips ? cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutStrips, UKT, SLOTS>, wmap, xmap, p)
+                : cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutTiles, UKT, SLOTS>, wmap, xmap, p);
 }
 
 // One pass of 17 to 128 rows.
@@ -402,20 +450,10 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
-  cudaError_t e = strips ? tc_smem_attr<BITS, kLayoutStrips, UKT>() : tc_smem_attr<BITS, kLayoutTiles, UKT>();
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ws.ctas);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = TcCfg<BITS>::kBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return strips ? cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutStrips, UKT>, wmap, xmap, p)
-                : cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutTiles, UKT>, wmap, xmap, p);
+  const int ns = tc_row_slots(lp.rows);
+  if (ns <= 32) return launch_tc<BITS, UKT, 32>(wmap, xmap, p, strips, ws.ctas, stream);
+  if (ns <= 64) return launch_tc<BITS, UKT, 64>(wmap, xmap, p, strips, ws.ctas, stream);
+  return launch_tc<BITS, UKT, 128>(wmap, xmap, p, strips, ws.ctas, stream);
 }
 
 }  // namespace
