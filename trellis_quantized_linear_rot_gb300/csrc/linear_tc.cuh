@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int issued = 0;
       for (int q = 0; q < n_half; ++q) {
         const int s = q % S;
-        if (q >= S && !mbar_wait_sleepy(empty_bar(s), ((q / S) - 1) & 1, abort_flag, 128)) break;
+        // A plain wait: the refill of a stage is on the decode warps' path.
+        if (q >= S && !mbar_wait(empty_bar(s), ((q / S) - 1) & 1, abort_flag)) break;
         const int h = q % H;
         const int kt0 = cur.ub() * UKT + h * kTcHalfKt;  // first k-tile of the half-unit
         const uint32_t st = smem_u32(smem + s * T::kStageBytes);
