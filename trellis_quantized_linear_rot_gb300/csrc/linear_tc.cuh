@@ -23,15 +23,17 @@
 //               Memory, added, written to this CTA's partial-sum slot, then
 //               (when the CTA owns the block, or arrives last) the output
 //               rotation, svh and the stores
-//   warps 4-19  decode: four warpgroups take half-units (8 k-tiles) in turn;
+//   warps 4-15  decode: three warpgroups (passes of up to 64 row slots;
+//               warps 4-19, four warpgroups, at 128) take half-units (8
+//               k-tiles) in turn;
 //               thread n decodes output n's 16 weights of each k-tile into
 //               Tensor Memory lane n (the MMA's A operand)
-//   warp 20     producer: the copies of each half-unit into a ring of
+//   next warp   producer: the copies of each half-unit into a ring of
 //               stages sized by the pass's row-slot class (packed weights, and
 //               the xr slice of the pass's row slots: two tensor copies of
 //               64 inputs x N rows with the 128-byte swizzle, which is the
 //               MMA's K-major B layout)
-//   warp 21     MMA: allocates Tensor Memory; the warp runs the MMA loop and
+//   last warp   MMA: allocates Tensor Memory; the warp runs the MMA loop and
 //               one elected lane issues
 // All waits are bounded; a kernel that gives up sets the error flag and exits.
 #pragma once
@@ -44,10 +46,6 @@ namespace {
 
 constexpr int kTcRows = 128;     // row slots of a pass (the MMA's N)
 constexpr int kTcHalfKt = 8;     // k-tiles per staged half-unit
-constexpr int kTcWG = 4;           // decode warpgroups
-constexpr int kTcProducer = 4 + 4 * kTcWG;
-constexpr int kTcMma = kTcProducer + 1;
-constexpr int kTcThreads = (kTcMma + 1) * 32;
 constexpr int kTcTmemCols = 512;  // acc[2] at columns 0 and 128; one A buffer per warpgroup at 256 + 64 wg
 constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared block
 
@@ -64,10 +62,17 @@ struct TcCfg {
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
   // to the same decode warpgroup.
-  static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) / kTcWG * kTcWG;
+  // Decode warpgroups: three up to 64 row slots, where the decode warps
+  // mostly wait and fewer of them leave the MMA and producer warps more issue
+  // slots and more stages fit; four at 128 slots (measured at 4 and 6 bits).
+  static constexpr int kWG = SLOTS <= 64 ? 3 : 4;
+  static constexpr int kProducer = 4 + 4 * kWG;  // warp roles: epilogue 0-3, decode, producer, MMA
+  static constexpr int kMma = kProducer + 1;
+  static constexpr int kThreads = (kMma + 1) * 32;
+  static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) / kWG * kWG;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
-  static constexpr int kNumBars = 2 * kStages + 2 * kTcWG + 3;  // full, empty, afull, aempty, dfull, dempty, drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kWG + 3;  // full, empty, afull, aempty, dfull, dempty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
 };
@@ -87,12 +92,15 @@ __device__ __forceinline__ void tc_decode_kt(const ColQuads<BITS>& cq, int col, 
 __host__ __device__ constexpr int tc_row_slots(int rows) { return (rows + 15) & ~15; }
 
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                              const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
   using T = TcCfg<BITS, SLOTS>;
   constexpr int S = T::kStages;
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
+  constexpr int kTcWG = T::kWG;
+  constexpr int kTcProducer = T::kProducer;
+  constexpr int kTcMma = T::kMma;
   static_assert(S >= kTcWG && S % kTcWG == 0, "stages must stay with one decode warpgroup");
   extern __shared__ __align__(1024) uint8_t smem[];
   float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + T::kXchOff);
@@ -396,7 +404,7 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, const Mm
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(TcCfg<BITS, SLOTS>::kThreads);
   cfg.dynamicSmemBytes = TcCfg<BITS, SLOTS>::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
