@@ -57,6 +57,30 @@ def test_noalloc_matches_regular_entry_point_twice(i_f, o_f, bits, rows):
     assert_close_f32(got[:, cols], ref)
 
 
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
+def test_noalloc_mma_kernel_bit_equal_to_tcgen05_kernel(bits):
+    """The no-allocation entry point runs every pass on the mma.sync kernel;
+    the regular entry point runs the k-tile order on the tcgen05 kernel. Both
+    give the same bits for every output, at 1, 8 and 16 rows and at every
+    width (2048 -> 8192: several units per CTA and blocks shared between
+    CTAs)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    i_f, o_f = 2048, 8192
+    tr = synth.make_trellis(i_f, o_f, bits, 910 + bits)
+    suh = synth.make_scale(i_f, 920 + bits)
+    svh = synth.make_scale(o_f, 930 + bits)
+    tr_t, svh_t = dev(tr), dev(svh)
+    for rows in (1, 8, 16):
+        xr_t = tf.tf_rot_in(dev(synth.make_x(rows, i_f, 940 + rows)), dev(suh))
+        want = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)).view(np.uint32)
+        y_t = torch.full((rows, o_f), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call_noalloc(xr_t, tr_t, svh_t, y_t, bits, rows, i_f, o_f) == tf.TF_OK
+        tf.tf_device_error()
+        got = host(y_t).view(np.uint32)
+        assert np.array_equal(got, want), "bits %d, %d rows: the two kernels differ" % (bits, rows)
+
+
 def test_noalloc_refuses_more_outputs_than_its_array_holds():
     lib = tf.lib()
     p = ctypes.c_void_p(0x10000)
