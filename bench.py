@@ -91,11 +91,41 @@ def alu_peak_tops(num_sms):
     return num_sms * 4 * 32 * max_sm_mhz() * 1e6 / 1e12
 
 
-def kernel_hash():
+def code_only(text):
+    """C++/CUDA source without its comments, trailing blanks and empty lines,
+    so that the kernel hash changes with the code and not with its comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
+def kernel_hash(read=None):
+    """Hash of the kernel sources' code (comments excluded). `read(name)`
+    returns a source's text (default: the files in csrc/)."""
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "trellis_quantized_linear_rot_gb300", "csrc", name), encoding="utf-8") as fh:
+                return fh.read()
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "trellis_quantized_linear_rot_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        h.update(code_only(read(f)).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -366,9 +366,10 @@ def test_host_pointer_is_refused():
                                               (4, 128, "strips"), (6, 100, "tiles"), (2, 129, "strips"),
                                               (8, 64, "strips"), (3, 200, "tiles"), (5, 96, "strips")])
 def test_prompt_pass_rows_bit_equal_to_decode_rows(bits, rows, layout):
-    """Passes of 17 to 128 rows (the tcgen05 kernel) give every row the same
-    bits as its run alone and as its 16-row pass (the mma.sync kernel), and
-    match the oracle; wkv shape 6144 -> 25,600."""
+    """Passes of 17 to 200 rows (up to 128 per pass, on the tcgen05 kernel)
+    give every row the same bits as its run alone and as its 16-row pass
+    (on whichever kernel the dispatch picks for those), and match the
+    oracle; wkv shape 6144 -> 25,600."""
     i_f, o_f = 6144, 25600
     x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=60 + bits)
     tr_t, svh_t = dev(tr), dev(svh)

@@ -92,7 +92,7 @@ struct MmaParams {
   const uint8_t* strips;  // packed weights in strips order (strips layout only)
   const __half* svh;
   void* y;
-  float* partials;      // [ctas][2][row slots][128]
+  float* partials;      // this kernel: [ctas][2][16][128]; the tcgen05 kernel: [ctas][3][128][128]
   int* counters;        // [out_features / 128]
   int* err_flag;
   long long units;      // (out/128) * (in/128)
@@ -612,9 +612,9 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
   }
   {
     // xr [rows][in] fp16 viewed as (64 inputs, rows, in / 64): a box of
-    // (64, slots, UKT / 4) lands as UKT / 4 chunks of 64 inputs, each of 16
-    // row slots (passes of up to 16 rows) or 32, 128 bytes per row, with the
-    // 128-byte swizzle; slots past `rows` are zero.
+    // (64, 16, UKT / 4) lands as UKT / 4 chunks of 64 inputs, each of 16
+    // row slots, 128 bytes per row, with the 128-byte swizzle; slots past
+    // `rows` are zero.
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows),
                                 static_cast<cuuint64_t>(lp.in_features / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};

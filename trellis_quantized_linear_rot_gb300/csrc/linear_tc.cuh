@@ -1,4 +1,5 @@
-// The trellis linear for prompt-sized passes (17 to 128 rows) on GB300:
+// The trellis linear for passes of up to 128 rows on GB300 (prompts, and the
+// decode passes the mma.sync kernel is slower at):
 // tcgen05 MMAs with the decoded weights in Tensor Memory, the same results
 // bit for bit as the decode-row kernel (linear_mma.cuh).
 //
@@ -413,7 +414,7 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, const Mm
                 : cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutTiles, UKT, SLOTS>, wmap, xmap, p);
 }
 
-// One pass of 17 to 128 rows.
+// One pass of up to 128 rows.
 template <int BITS, int UKT>
 cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   auto encode = encode_fn();
