@@ -186,7 +186,10 @@ tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* 
  * before capturing work into a CUDA graph). Each call clears the counters it
  * uses with cudaMemsetAsync on `stream`. All calls share the one array, so
  * calls whose work overlaps on the GPU (for example on two streams) race and
- * must be ordered by the caller. Calls no cudaMalloc or cudaFree.
+ * must be ordered by the caller. Calls no cudaMalloc or cudaFree. It runs
+ * its passes of up to 16 rows on the mma.sync kernel (whose partial sums fit
+ * the array); every output has the same bits as tf_trellis_linear's, which
+ * may run the same pass on the tcgen05 kernel.
  */
 tf_status tf_trellis_linear_noalloc(const void* xr, const void* trellis, const void* svh,
                                     void* y, int out_dtype, int rows, int in_features,
