@@ -291,6 +291,15 @@ class OraclePool:
         self.pool.join()
 
 
+def bench_config(args, world):
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F, "out_features": OUT_F,
+            "bits": BITS, "out_dtype": "fp32", "weight_bytes_per_call": weight_bytes(),
+            "layout": args.layout,
+            "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     """The oracle timed on the host cores, on the same workload and metric.
     Each step is a bounded sample of it (one output block over a slice of the
@@ -318,8 +327,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F,
-                                        "out_features": OUT_F, "bits": BITS},
+        "data": "synthetic", "config": bench_config(args, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
                          "sample": sample, "host_threads_available": cpu_threads()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -471,11 +479,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 (fp32 sums)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F, "out_features": OUT_F,
-                   "bits": BITS, "out_dtype": "fp32", "weight_bytes_per_call": weight_bytes(),
-                   "layout": args.layout,
-                   "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(args, world),
         "by_rows": per_rows,
         "roofline": {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
                      "frac": alu_achieved / alu_peak, "traffic": traffic,
