@@ -52,7 +52,7 @@ constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared bloc
 
 // Shared memory of a pass class: stages of a half-unit's packed weights and
 // its xr slice for up to SLOTS row slots (32, 64 or 128). Fewer slots make
-// smaller stages and so more of them in flight: 12 / 8 / 4 at 4 bits (the
+// smaller stages and so more of them in flight: 12 / 9 / 4 at 4 bits (the
 // copies of a stage take longer to land than a warpgroup takes to decode
 // one half-unit, so a warpgroup needs stages beyond the one it decodes).
 template <int BITS, int SLOTS>
