@@ -1,0 +1,302 @@
+"""The two linear kernels' barrier protocols, simulated on the host under
+random schedules.
+
+Every role of a CTA (producer, decode or compute warps, MMA warp, epilogue) is
+a generator that runs the same index arithmetic as the kernel and waits on
+simulated mbarriers with the kernel's parities. An mbarrier completes a phase
+when its expected arrivals and transaction bytes are in; a parity wait passes
+while the barrier's current phase has the other parity, which is how
+`mbarrier.try_wait.parity` behaves. Copies land in any order; tensor-core work
+(the tcgen05 kernel's MMAs and their commits) completes in issue order at
+random later times. Every buffer carries a tag naming the unit, half-unit or
+segment whose data it holds, and every read and every asynchronous MMA checks
+the tag: a wait that passed on a stale phase, a stage refilled while still
+being read, or an accumulator reused too early fails the test. A schedule that
+leaves work undone with nothing runnable is a deadlock and fails too.
+
+A planted fault (a stage count that is not a multiple of the consumers, the
+kind of assignment that once let a wait run two phases ahead) must be caught.
+"""
+
+import random
+
+import pytest
+
+from test_pipeline_cpu import SegmentOrder, ranges
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.tx, self.phase = name, count, count, 0, 0
+
+    def arrive(self, n=1):
+        assert self.pending >= n, "%s: more arrivals than the phase expects" % self.name
+        self.pending -= n
+        self._complete()
+
+    def arrive_expect_tx(self, nbytes):
+        self.tx += nbytes
+        self.arrive()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        assert self.tx >= 0, "%s: bytes beyond the expected count" % self.name
+        self._complete()
+
+    def _complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def passes(self, parity):
+        return (self.phase & 1) != parity
+
+
+class Sim:
+    """Random scheduler over role generators and asynchronous events."""
+
+    def __init__(self, rng):
+        self.rng = rng
+        self.roles = []          # [generator, pending wait or None]
+        self.copies = []         # copies in flight: callables, land in any order
+        self.tensor = []         # tensor-core queue: callables, complete in order
+
+    def add(self, gen):
+        self.roles.append([gen, None])
+
+    def run(self, max_steps=2_000_000):
+        for _ in range(max_steps):
+            ready = [r for r in self.roles if r[1] is None or r[1][0].passes(r[1][1])]
+            events = len(self.copies) + (1 if self.tensor else 0)
+            if not ready and not events:
+                if self.roles:
+                    names = [r[1][0].name for r in self.roles if r[1] is not None]
+                    raise AssertionError("deadlock: roles wait on %s" % names)
+                return
+            pick = self.rng.randrange(len(ready) + events)
+            if pick < len(ready):
+                role = ready[pick]
+                try:
+                    role[1] = next(role[0])
+                except StopIteration:
+                    self.roles.remove(role)
+            elif pick - len(ready) < len(self.copies):
+                self.copies.pop(pick - len(ready))()
+            else:
+                self.tensor.pop(0)()
+        raise AssertionError("schedule did not finish")
+
+
+def wait(bar, parity):
+    """Yield point of a role: resumes once `bar` passes `parity`."""
+    return (bar, parity)
+
+
+# --------------------------------------------------------------------------
+# The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
+
+def run_tc(order, S, WG, H, rng):
+    sim = Sim(rng)
+    n_half = order.n_units * H
+    full = [Bar("full%d" % s, 1) for s in range(S)]
+    empty = [Bar("empty%d" % s, 4 + 1) for s in range(S)]
+    afull = [Bar("afull%d" % w, 4) for w in range(WG)]
+    aempty = [Bar("aempty%d" % w, 1) for w in range(WG)]
+    dfull, dempty = Bar("dfull", 1), Bar("dempty", 4)
+    stage = [None] * S       # half-unit whose copy the stage holds
+    abuf = [None] * WG       # half-unit whose decoded weights the A buffer holds
+    acc = [None]             # segment whose sums the accumulators hold
+    STAGE_BYTES = 3
+
+    def producer():
+        for q in range(n_half):
+            s = q % S
+            if q >= S:
+                yield wait(empty[s], ((q // S) - 1) & 1)
+            full[s].arrive_expect_tx(STAGE_BYTES)
+
+            def land(s=s, q=q):
+                stage[s] = q
+                full[s].complete_tx(STAGE_BYTES)
+            sim.copies.append(land)
+
+    def decode(wg):
+        j = 0
+        while WG * j + wg < n_half:
+            q = WG * j + wg
+            s = q % S
+            yield wait(full[s], (q // S) & 1)
+            if j >= 1:
+                yield wait(aempty[wg], (j - 1) & 1)
+            assert stage[s] == q, "decode of %d read stage %d holding %s" % (q, s, stage[s])
+            abuf[wg] = q
+            yield None                                    # the decode takes a while
+            assert stage[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
+            for _ in range(4):
+                afull[wg].arrive()
+                empty[s].arrive()
+            j += 1
+
+    def mma():
+        for sg in range(order.n_seg):
+            bb = order.block(sg)
+            seg_lo, seg_hi = order.lo(bb), order.hi(bb)
+            base = order.pos(sg, seg_lo) - seg_lo
+            if sg >= 1:
+                yield wait(dempty, (sg - 1) & 1)
+            for i in range(seg_lo, seg_hi):
+                for h in range(H):
+                    q = (base + i) * H + h
+                    s, wg, j = q % S, q % WG, q // WG
+                    yield wait(full[s], (q // S) & 1)
+                    yield wait(afull[wg], j & 1)
+
+                    def execute(q=q, s=s, wg=wg, sg=sg):
+                        assert stage[s] == q, "MMA of %d found stage %d holding %s" % (q, s, stage[s])
+                        assert abuf[wg] == q, "MMA of %d found A buffer %d holding %s" % (q, wg, abuf[wg])
+                        acc[0] = sg
+                        aempty[wg].arrive()                  # the two commits after the MMAs
+                        empty[s].arrive()
+                    sim.tensor.append(execute)
+            sim.tensor.append(dfull.arrive)                  # commit at the segment's end
+
+    def epilogue():
+        for sg in range(order.n_seg):
+            yield wait(dfull, sg & 1)
+            assert acc[0] == sg, "segment %d read accumulators of %s" % (sg, acc[0])
+            yield None                                    # the readout takes a while
+            assert acc[0] == sg, "accumulators of segment %d overwritten during readout" % sg
+            for _ in range(4):
+                dempty.arrive()
+
+    sim.add(producer())
+    for wg in range(WG):
+        sim.add(decode(wg))
+    sim.add(mma())
+    sim.add(epilogue())
+    sim.run()
+    assert all(stage[s] is not None for s in range(min(S, n_half)))
+
+
+# --------------------------------------------------------------------------
+# The mma.sync kernel: producer, two compute groups, epilogue.
+
+def run_mma(order, S, rng, groups=2):
+    sim = Sim(rng)
+    n = order.n_units
+    full = [Bar("full%d" % s, 1) for s in range(S)]
+    empty = [Bar("empty%d" % s, 1) for s in range(S)]   # one arrival per group here (8 warps in the kernel)
+    dfull = [Bar("dfull%d" % d, groups) for d in range(2)]
+    dempty = [Bar("dempty%d" % d, 1) for d in range(2)]
+    stage = [None] * S
+    dbuf = [[None] * groups for _ in range(2)]
+    prod = []
+    for q in range(order.n_seg):
+        bb = order.block(q)
+        prod.extend(order.u0 + i for i in range(order.lo(bb), order.hi(bb)))
+
+    def producer():
+        for k in range(n):
+            s = k % S
+            if k >= S:
+                yield wait(empty[s], ((k // S) - 1) & 1)
+            full[s].arrive_expect_tx(1)
+
+            def land(s=s, k=k):
+                stage[s] = prod[k]
+                full[s].complete_tx(1)
+            sim.copies.append(land)
+
+    def compute(cg):
+        for sg in range(order.n_seg):
+            bb = order.block(sg)
+            seg_lo, seg_hi = order.lo(bb), order.hi(bb)
+            base = order.pos(sg, seg_lo) - seg_lo
+            i = seg_lo + ((cg - base - seg_lo) % groups)
+            while i < seg_hi:
+                k = base + i
+                s = k % S
+                yield wait(full[s], (k // S) & 1)
+                assert stage[s] == order.u0 + i, "group %d read stage %d holding unit %s, wanted %d" % (
+                    cg, s, stage[s], order.u0 + i)
+                yield None
+                assert stage[s] == order.u0 + i, "stage %d refilled during its unit" % s
+                empty[s].arrive()
+                i += groups
+            d = sg & 1
+            if sg >= 2:
+                yield wait(dempty[d], ((sg >> 1) - 1) & 1)
+            dbuf[d][cg] = sg
+            dfull[d].arrive()
+
+    def epilogue():
+        for sg in range(order.n_seg):
+            d = sg & 1
+            yield wait(dfull[d], (sg >> 1) & 1)
+            assert dbuf[d] == [sg] * groups, "segment %d read sums %s" % (sg, dbuf[d])
+            yield None
+            assert dbuf[d] == [sg] * groups, "sums of segment %d overwritten" % sg
+            dempty[d].arrive()
+
+    sim.add(producer())
+    for cg in range(groups):
+        sim.add(compute(cg))
+    sim.add(epilogue())
+    sim.run()
+
+
+def cta_orders(seed, n):
+    rng = random.Random(seed)
+    for _ in range(n):
+        ub = rng.choice([1, 2, 3, 5, 10, 20])
+        units = ub * rng.randint(1, 12)
+        ctas = min(units, rng.choice([1, 2, 3, 5, 7]))
+        c = rng.randrange(ctas)
+        u0, u1 = ranges(units, ctas)[c]
+        yield SegmentOrder(u0, u1, ub)
+
+
+@pytest.mark.parametrize("S,WG,H", [(12, 3, 2), (9, 3, 2), (6, 3, 1), (4, 4, 2), (8, 4, 1)])
+def test_tc_kernel_protocol_under_random_schedules(S, WG, H):
+    rng = random.Random(100 * S + 10 * WG + H)
+    for order in cta_orders(S * WG + H, 60):
+        for _ in range(3):
+            run_tc(order, S, WG, H, rng)
+
+
+@pytest.mark.parametrize("S", [4, 6, 8, 12])
+def test_mma_kernel_protocol_under_random_schedules(S):
+    rng = random.Random(S)
+    for order in cta_orders(50 + S, 80):
+        for _ in range(3):
+            run_mma(order, S, rng)
+
+
+def test_planted_fault_is_caught():
+    """Stages that are not a multiple of the consumers: a stage's previous
+    half-unit went to another warpgroup, which can still be reading it when
+    its new copy is ordered, and a parity wait can pass on the wrong phase.
+    Some schedule must fail."""
+    rng = random.Random(7)
+    failures = 0
+    for order in cta_orders(7, 40):
+        for _ in range(5):
+            try:
+                run_tc(order, 5, 4, 2, rng)
+            except AssertionError:
+                failures += 1
+    assert failures > 0
+
+
+def test_planted_fault_in_the_mma_kernel_is_caught():
+    """An odd stage count in the mma.sync kernel: unit k and unit k - S go to
+    different groups."""
+    rng = random.Random(8)
+    failures = 0
+    for order in cta_orders(8, 40):
+        for _ in range(5):
+            try:
+                run_mma(order, 5, rng)
+            except AssertionError:
+                failures += 1
+    assert failures > 0
