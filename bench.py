@@ -13,16 +13,16 @@ from the k-tile-major tiles at load time, outside the timed region;
 (331 MB each) exceed the 129 MB L2; two copies alternate between calls, so no
 call finds its weights in L2.
 
-Metric: weight GB/s = packed weight bytes streamed / time, with the fraction
-of the measured HBM copy bandwidth it reaches. Prints one JSON line.
+Metric: weight GB/s = packed weight bytes streamed / time. The roofline is
+HBM: the fraction is the linear's algorithmic bytes per launch (packed
+weights + xr + svh + y) over its CUDA-event time, against the measured HBM
+copy bandwidth. The decode's issue-slot view (lane operations per second
+against the SMs' issue peak) is reported beside it under "alu".
 
-Roofline: the linear is bound by the decode's integer arithmetic, not by HBM.
-Decoding one weight takes four 32-bit lane operations (cut its 16-bit window
-out of the stream, multiply by the mul1 constant, sum the product's bytes, one
-fp16 fma); an SM issues one warp instruction (32 lane operations) per cycle in
-each of its four sub-partitions, so the peak is SMs x 4 x 32 x the maximum SM
-clock. The line's "roofline" reports that bound (unit: tera lane-ops/s) and,
-under "hbm", the fraction of the measured copy bandwidth.
+Also measured in the same run, outside the headline: every other
+configuration the page's projections give (wk, wkv at 1/4/16 rows, the bit
+width sweep at 8 rows, the head at 6 bits and 64 rows) under "by_config",
+each with time, weight GB/s, rows/s and the HBM fraction.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,6 +33,7 @@ replicas (weak scaling) and rank 0 reports the aggregate.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -49,16 +50,33 @@ WORKLOAD = "LM head 5120->129280, 4 bits/weight, rows {1,8,16} per step, fp32 lo
 METRIC = "weight GB/s and % of HBM peak, trellis linear 5120->129280 @4b, 1-16 rows"
 KERNEL_SOURCES = ("linear_mma.cu", "linear_mma.cuh", "linear_tc.cuh", "decode.cuh", "epilogue.cuh", "ptx.cuh",
                   "kernels.h")
+DOMINANT_KERNEL = "trellis_linear_tc_kernel"
+L2_BYTES = 129 * 1024 * 1024
+
+# The other configurations of the page's projections, timed in the same run
+# (not part of the headline): (name, in, out, bits, rows, out dtype).
+CONFIGS = [
+    ("wk 512->128", 512, 128, 4, (1,), "fp16"),
+    ("wkv 6144->25600", 6144, 25600, 4, (1, 4, 16), "fp16"),
+    ("wkv sweep 2b", 6144, 25600, 2, (8,), "fp16"),
+    ("wkv sweep 3b", 6144, 25600, 3, (8,), "fp16"),
+    ("wkv sweep 4b", 6144, 25600, 4, (8,), "fp16"),
+    ("wkv sweep 5b", 6144, 25600, 5, (8,), "fp16"),
+    ("wkv sweep 6b", 6144, 25600, 6, (8,), "fp16"),
+    ("wkv sweep 8b", 6144, 25600, 8, (8,), "fp16"),
+    ("head 6b", 5120, 129280, 6, (64,), "fp32"),
+]
 
 
-def weight_bytes():
-    return IN_F * OUT_F * BITS // 8
+def weight_bytes(i=IN_F, o=OUT_F, b=BITS):
+    return i * o * b // 8
 
 
-def launch_bytes(rows):
-    """Algorithmic bytes of one linear launch: packed weights, fp16 xr, fp16
-    svh, fp32 y."""
-    return weight_bytes() + rows * IN_F * 2 + OUT_F * 2 + rows * OUT_F * 4
+def launch_bytes(rows, i=IN_F, o=OUT_F, b=BITS, out_elem=4):
+    """Algorithmic bytes of one linear call: packed weights (streamed once per
+    pass of up to 128 rows), fp16 xr, fp16 svh, the output."""
+    passes = max(1, math.ceil(rows / 128))
+    return passes * weight_bytes(i, o, b) + rows * i * 2 + o * 2 + rows * o * out_elem
 
 
 # Lane operations the method's decode needs per weight: window cut, 32-bit
@@ -66,22 +84,25 @@ def launch_bytes(rows):
 DECODE_OPS_PER_WEIGHT = 4
 
 
-def measured_peaks():
+def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as fh:
-            d = json.load(fh)
+            return json.load(fh)
+    return None
+
+
+def measured_peaks():
+    d = _peaks()
+    if d is not None:
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
 
 
 def max_sm_mhz():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        with open(path) as fh:
-            d = json.load(fh)
-        if d.get("sm_max_mhz"):
-            return float(d["sm_max_mhz"])
+    d = _peaks()
+    if d is not None and d.get("sm_max_mhz"):
+        return float(d["sm_max_mhz"])
     return 2070.0
 
 
@@ -130,8 +151,9 @@ def kernel_hash(read=None):
 
 
 def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources (else None).
+    Returns {rows: bytes}."""
     path = os.path.join(ROOT, "profiles", "trellis_linear_head_4b.json")
     if not os.path.exists(path):
         return None
@@ -139,7 +161,10 @@ def profiled_traffic():
         d = json.load(fh)
     if d.get("kernel_hash") != kernel_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    per = d.get("dram_bytes_per_launch_by_rows")
+    if isinstance(per, dict):
+        return {int(k): v for k, v in per.items()}
+    return None
 
 
 class ClockSampler:
@@ -158,7 +183,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -220,28 +245,28 @@ def dist_env():
     return world, rank, local
 
 
-def oracle_sample(n_blocks, rows_list, k_tiles=IN_F // 16, stream=0):
-    """The oracle on a bounded sample of the workload: the weights of n_blocks
-    output blocks of 128 over the first k_tiles * 16 inputs (decoded from a
-    packed stream of the same distribution; `stream` picks another seeded
-    stream), for each row count: rot_in, decode, float64 linear and output
-    rotation. Returns (seconds, packed weight bytes covered)."""
+# ------------------------------------------------------------ CPU baseline
+def oracle_sample(n_blocks, rows_list, stream=0):
+    """The oracle on a bounded sample of the workload: n_blocks output blocks
+    of 128 over all 5120 inputs (a packed stream of the same distribution,
+    `stream` picking another seeded one), for each row count: rot_in,
+    decode, float64 linear and output rotation. Returns (seconds, packed
+    weight bytes covered)."""
     import numpy as np
     from oracle import exl3 as o
     from trellis_quantized_linear_rot_gb300 import synth
-    i_s = 128 * max(1, k_tiles // 8)
     g = np.random.Generator(np.random.PCG64(synth.SEED_TRELLIS + 2 + BITS + 1000 * stream))
-    tr = g.integers(0, 2**32, size=i_s * 128 * n_blocks * BITS // 32, dtype=np.uint32)
-    x = synth.make_x(max(rows_list), i_s, synth.SEED_X + 2)
-    suh = synth.make_scale(i_s, synth.SEED_SUH + 2)
+    tr = g.integers(0, 2**32, size=IN_F * 128 * n_blocks * BITS // 32, dtype=np.uint32)
+    x = synth.make_x(max(rows_list), IN_F, synth.SEED_X + 2)
+    suh = synth.make_scale(IN_F, synth.SEED_SUH + 2)
     svh = synth.make_scale(128 * n_blocks, synth.SEED_SVH + 2)
     t0 = time.perf_counter()
     covered = 0
     for rows in rows_list:
         xr = o.rot_in_f32(x[:rows], suh)
-        w = o.decode_matrix(tr, i_s, 128 * n_blocks, BITS)
+        w = o.decode_matrix(tr, IN_F, 128 * n_blocks, BITS)
         o.linear_f64(xr, w, svh)
-        covered += i_s * 128 * n_blocks * BITS // 8
+        covered += weight_bytes(IN_F, 128 * n_blocks)
     return time.perf_counter() - t0, covered
 
 
@@ -257,9 +282,10 @@ def _oracle_job(job):
 
 
 class OraclePool:
-    """The oracle on every host core: one worker process per core, started
-    with spawn (never forked from a process that has used the GPU), each with
-    its BLAS limited to one thread, each timing its own seeded sample."""
+    """The oracle on `workers` host cores: one worker process per core,
+    started with spawn (never forked from a process that has used the GPU),
+    each with its BLAS limited to one thread, each timing its own seeded
+    sample."""
 
     ONE_THREAD = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
@@ -277,11 +303,12 @@ class OraclePool:
                     os.environ.pop(k, None)
                 else:
                     os.environ[k] = v
-        self.run(1, ROWS[:1], 8)  # imports in every worker
+        self.run(1)  # imports in every worker
 
-    def run(self, n_blocks_each, rows_list, k_tiles):
+    def run(self, n_blocks_each, rows_list=None):
         """Wall seconds for all workers' samples, and the bytes they covered."""
-        jobs = [(n_blocks_each, tuple(rows_list), k_tiles, w) for w in range(self.workers)]
+        rows_list = tuple(rows_list or ROWS)
+        jobs = [(n_blocks_each, rows_list, w) for w in range(self.workers)]
         t0 = time.perf_counter()
         res = self.pool.map(_oracle_job, jobs)
         return time.perf_counter() - t0, sum(r[1] for r in res)
@@ -289,6 +316,29 @@ class OraclePool:
     def close(self):
         self.pool.close()
         self.pool.join()
+
+
+def sample_text(n_blocks, workers):
+    return ("per worker: %d of 1010 output blocks (5120x128 weights each) for each of rows {%s}; "
+            "%d single-threaded worker%s" % (n_blocks, ",".join(str(r) for r in ROWS), workers,
+                                              "" if workers == 1 else "s"))
+
+
+def cpu_baseline(all_blocks=60, one_blocks=6):
+    """The oracle's weight GB/s on every host core (one single-threaded worker
+    per core) and on one core, on the same sample definition as the
+    reference arm."""
+    pool = OraclePool(cpu_threads())
+    secs, covered = pool.run(all_blocks)
+    pool.close()
+    one = OraclePool(1)
+    secs1, covered1 = one.run(one_blocks)
+    one.close()
+    return {"value": covered / secs / 1e9, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
+            "sample": sample_text(all_blocks, pool.workers) + ", %.1f s wall" % secs,
+            "host_threads_available": cpu_threads(),
+            "one_core": {"value": covered1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
+                         "sample": sample_text(one_blocks, 1) + ", %.1f s wall" % secs1}}
 
 
 def bench_config(args, world):
@@ -301,38 +351,85 @@ def bench_config(args, world):
 
 
 def run_reference(args):
-    """The oracle timed on the host cores, on the same workload and metric.
-    Each step is a bounded sample of it (one output block over a slice of the
-    inputs, for each row count), sized so that the whole run of warm-up and
-    timed steps takes about two minutes."""
+    """The oracle timed on the host cores, on the same workload and metric:
+    each step is the same bounded sample as the cpu_baseline leg of our arm
+    (whole output blocks over all inputs, for each row count), with the block
+    count sized so that the whole run of warm-up and timed steps takes about
+    two minutes."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
     pool = OraclePool(cpu_threads())
-    t_cal, _ = pool.run(1, ROWS, 8)                    # 128 inputs x 128 outputs per worker
+    t_cal, _ = pool.run(1)
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    k_tiles = int(max(8, min(IN_F // 16, 8 * per_step / max(t_cal, 1e-6))))
+    n_blocks = int(max(1, min(60, per_step / max(t_cal, 1e-6))))
     for _ in range(args.warmup):
-        pool.run(1, ROWS, k_tiles)
+        pool.run(n_blocks)
     total_t, total_b = 0.0, 0
     for _ in range(args.steps):
-        t, b = pool.run(1, ROWS, k_tiles)
+        t, b = pool.run(n_blocks)
         total_t += t
         total_b += b
     pool.close()
     value = total_b / total_t / 1e9
-    sample = ("per worker and step: 1 of 1010 output blocks over %d of 5120 inputs per row count "
-              "(rows {1,8,16}); %d single-threaded workers" % (128 * max(1, k_tiles // 8), pool.workers))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": bench_config(args, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
-                         "sample": sample, "host_threads_available": cpu_threads()},
+                         "sample": sample_text(n_blocks, pool.workers) + " per step",
+                         "host_threads_available": cpu_threads()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ GPU arm
+def time_config(tf, dev, name, i_f, o_f, bits, rows_list, out_dtype, layout, iters, peak):
+    """One configuration: the linear alone (xr already rotated), weight
+    copies alternated so that their total exceeds twice the L2. Returns
+    {rows: figures}."""
+    import numpy as np
+    import torch
+    from trellis_quantized_linear_rot_gb300 import synth
+    c = [c[0] for c in CONFIGS].index(name)
+    w0 = torch.from_numpy(synth.make_trellis(i_f, o_f, bits, synth.SEED_TRELLIS + 10 + c).view(np.int32)).to(dev)
+    if layout == "strips":
+        w0 = tf.tf_trellis_to_strips(w0, i_f, o_f, bits)
+    n_copies = max(2, math.ceil(2 * L2_BYTES / max(1, weight_bytes(i_f, o_f, bits))))
+    n_copies = min(n_copies, 64)
+    ws = [w0] + [w0.clone() for _ in range(n_copies - 1)]
+    lin = tf.tf_trellis_linear_strips if layout == "strips" else tf.tf_trellis_linear
+    R = max(rows_list)
+    x = torch.from_numpy(synth.make_x(R, i_f, synth.SEED_X + 10 + c)).to(dev)
+    suh = torch.from_numpy(synth.make_scale(i_f, synth.SEED_SUH + 10 + c)).to(dev)
+    svh = torch.from_numpy(synth.make_scale(o_f, synth.SEED_SVH + 10 + c)).to(dev)
+    xr = tf.tf_rot_in(x, suh)
+    dt = {"fp16": torch.float16, "fp32": torch.float32}[out_dtype]
+    st = torch.cuda.current_stream()
+    out = {}
+    for r in rows_list:
+        y = torch.empty((r, o_f), dtype=dt, device=dev)
+        for k in range(3):
+            lin(xr[:r], ws[k % n_copies], svh, bits, o_f, y=y)
+        evs = []
+        for k in range(iters):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            lin(xr[:r], ws[k % n_copies], svh, bits, o_f, y=y)
+            e1.record(st)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        us = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+        lb = launch_bytes(r, i_f, o_f, bits, 2 if out_dtype == "fp16" else 4)
+        out[str(r)] = {"us_median": us, "weight_gbs": weight_bytes(i_f, o_f, bits) * math.ceil(r / 128) / us / 1e3,
+                       "rows_per_s": r / (us * 1e-6), "hbm_frac": lb / us / 1e3 / peak}
+    tf.tf_device_error()
+    del ws
+    return {"in_features": i_f, "out_features": o_f, "bits": bits, "out_dtype": out_dtype,
+            "weight_copies": n_copies, "by_rows": out}
 
 
 def run_ours(args):
@@ -363,7 +460,7 @@ def run_ours(args):
     tr1 = tr0.clone()
     linear = tf.tf_trellis_linear_strips if args.layout == "strips" else tf.tf_trellis_linear
     trs = (tr0, tr1)
-    x = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).to(dev)
+    x = torch.from_numpy(synth.make_x(max(ROWS), IN_F, synth.SEED_X + 2)).to(dev)
     suh = torch.from_numpy(synth.make_scale(IN_F, synth.SEED_SUH + 2)).to(dev)
     svh = torch.from_numpy(synth.make_scale(OUT_F, synth.SEED_SVH + 2)).to(dev)
     xrs = {r: torch.empty((r, IN_F), dtype=torch.float16, device=dev) for r in ROWS}
@@ -374,7 +471,8 @@ def run_ours(args):
     def step(record):
         # The event pair brackets rot_in and the linear: an event recorded
         # between them would cut the programmatic dependent launch that lets
-        # the linear's prologue overlap rot_in. rot_in is ~1 % of the pair.
+        # the linear's prologue overlap rot_in. rot_in is ~2 % of the pair,
+        # so the linear's figures below are slightly conservative.
         for r in ROWS:
             if record:
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -408,19 +506,22 @@ def run_ours(args):
     bytes_step = weight_bytes() * len(ROWS)
     value = replica_value(bytes_step, args.steps, world, ms_total)
 
-    # Dominant kernel: the linear launches, timed by events on their stream.
+    # The dominant kernel: the linear launches, timed by events on their
+    # stream over the timed region.
+    peak, peak_kind = measured_peaks()
     per_rows = {}
     dur_sum, byte_sum, launches = 0.0, 0, 0
     for r in ROWS:
         ds = [a.elapsed_time(b) for a, b in ev[r]]
-        per_rows[r] = {"us_median": statistics.median(ds) * 1e3,
-                       "weight_gbs": weight_bytes() / (statistics.median(ds) * 1e-3) / 1e9}
+        us = statistics.median(ds) * 1e3
+        per_rows[str(r)] = {"us_median": us, "weight_gbs": weight_bytes() / us / 1e3, "rows_per_s": r / (us * 1e-6),
+                            "hbm_gbs": launch_bytes(r) / us / 1e3, "hbm_frac": launch_bytes(r) / us / 1e3 / peak}
         dur_sum += sum(ds)
         byte_sum += launch_bytes(r) * len(ds)
         launches += len(ds)
     achieved = byte_sum / (dur_sum * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
     traffic = profiled_traffic()
+    traffic_avg = (sum(traffic[r] for r in ROWS) / len(ROWS)) if traffic and all(r in traffic for r in ROWS) else None
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = alu_peak_tops(num_sms)
     alu_achieved = IN_F * OUT_F * DECODE_OPS_PER_WEIGHT * launches / (dur_sum * 1e-3) / 1e12
@@ -429,7 +530,7 @@ def run_ours(args):
     # copies its rows of x in, and its logits out on a copy stream that waits
     # for the call, so that the read of one call's logits overlaps the next
     # call; the timed region ends when every copy has landed.
-    x_host = torch.from_numpy(synth.make_x(16, IN_F, synth.SEED_X + 2)).pin_memory()
+    x_host = torch.from_numpy(synth.make_x(max(ROWS), IN_F, synth.SEED_X + 2)).pin_memory()
     y_host = {r: torch.empty((r, OUT_F), dtype=torch.float32).pin_memory() for r in ROWS}
     e2e_steps = max(2, min(args.steps, 200))
     copy_stream = torch.cuda.Stream(device=dev)
@@ -460,6 +561,17 @@ def run_ours(args):
     e2e_s = max_over_ranks(e2e_s, dist, dev)
     e2e_value = replica_value(bytes_step, e2e_steps, world, e2e_s * 1e3) if not args.no_e2e else None
 
+    # The other configurations (untimed for the headline).
+    by_config = None
+    if not args.no_configs and rank == 0:
+        del trs, tr0, tr1
+        torch.cuda.empty_cache()
+        by_config = {}
+        for name, i_f, o_f, bits, rows_list, odt in CONFIGS:
+            by_config[name] = time_config(tf, dev, name, i_f, o_f, bits, rows_list, odt, args.layout,
+                                          args.config_iters, peak)
+            torch.cuda.empty_cache()
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -467,27 +579,20 @@ def run_ours(args):
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        n_blocks = 60
-        pool = OraclePool(cpu_threads())
-        secs, covered = pool.run(n_blocks, ROWS, IN_F // 16)
-        pool.close()
-        cpu = {"value": covered / secs / 1e9, "unit": "GB/s", "cores": pool.workers, "kind": "oracle",
-               "sample": "per worker: %d of 1010 output blocks (5120x128 weights each) for each of rows "
-                         "{1,8,16}; %d single-threaded workers, %.1f s wall" % (n_blocks, pool.workers, secs),
-               "host_threads_available": cpu_threads()}
+        cpu = cpu_baseline()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16 (fp32 sums)", "data": "synthetic",
         "config": bench_config(args, world),
         "by_rows": per_rows,
-        "roofline": {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
-                     "frac": alu_achieved / alu_peak, "traffic": traffic,
-                     "ops_per_weight": DECODE_OPS_PER_WEIGHT,
-                     "peak_source": "%d SMs x 4 issue slots x 32 lanes x %.0f MHz" % (num_sms, max_sm_mhz()),
-                     "kernel": "trellis_linear", "kernel_hash": kernel_hash(),
-                     "hbm": {"achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                             "peak_source": peak_kind}},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_avg, "peak_source": peak_kind,
+                     "kernel": DOMINANT_KERNEL, "kernel_hash": kernel_hash(),
+                     "bytes_per_launch": {str(r): launch_bytes(r) for r in ROWS},
+                     "alu": {"achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
+                             "frac": alu_achieved / alu_peak, "ops_per_weight": DECODE_OPS_PER_WEIGHT,
+                             "peak_source": "%d SMs x 4 issue slots x 32 lanes x %.0f MHz" % (num_sms, max_sm_mhz())}},
         "clocks": clocks.summary(),
         "e2e": None if args.no_e2e else {
             "value": e2e_value, "unit": "GB/s",
@@ -495,6 +600,7 @@ def run_ours(args):
             "d2h_bytes_per_step": sum(r * OUT_F * 4 for r in ROWS)},
         "gpu_launches": 2 * len(ROWS) * args.steps,
         "cpu_baseline": cpu,
+        "by_config": by_config,
     }
     print(json.dumps(line))
     if dist is not None:
@@ -509,6 +615,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations")
+    ap.add_argument("--config-iters", type=int, default=20)
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
     ap.add_argument("--layout", choices=["tiles", "strips"], default="strips",
                     help="weight storage order: strips (repacked once at load, untimed; the default) "

@@ -48,7 +48,8 @@ typedef enum {
 
 typedef enum { TF_F16 = 0, TF_F32 = 1, TF_BF16 = 2 } tf_dtype;
 
-/* Version of this ABI (incremented on any incompatible change). */
+/* Version of this ABI (incremented on any incompatible change). The pages
+ * have no counterpart: it is this library's own. */
 int tf_abi_version(void);
 
 /*
@@ -96,10 +97,8 @@ tf_status tf_rot_in(const void* x, int x_dtype, const void* suh, void* xr,
  *   (fp16 bit patterns; 0x1EEE = 0.00676727294921875, 0xC2E8 = -3.453125).
  * svh:     [out_features] fp16
  * y:       [rows][out_features], out_dtype TF_F16, TF_F32 or TF_BF16, written
- * rows >= 0 (0 launches nothing). Rows run in passes of up to 128 on one of
- * two kernels (an mma.sync kernel for passes of up to 8 rows at 2 to 5 bits
- * in the strips order, a tcgen05 kernel otherwise; the choice changes no
- * bit), each pass
+ * rows >= 0 (0 launches nothing). Rows run in passes of up to 128 on the
+ * tcgen05 kernel, each pass
  * decoding the weights once for all its rows ("Known limits": the prompt
  * path, registered bit-equal to this linear): a row's outputs are the same
  * bits whatever pass, slot or batch it runs in, alone or among up to 128
@@ -135,12 +134,16 @@ tf_status tf_trellis_linear_strips(const void* xr, const void* strips, const voi
  * tf_trellis_to_strips -- repacks tiles from the k-tile-major order of
  * tf_trellis_linear into the strips order of tf_trellis_linear_strips
  * (tf_trellis_bytes(in, out, bits) bytes each; the buffers must not overlap).
+ * "Checks on this head" names the two tile layouts the decode runs on; this
+ * repack between the library's own readings of them has no counterpart on
+ * the pages.
  */
 tf_status tf_trellis_to_strips(const void* tiles, void* strips, int in_features,
                                int out_features, int bits, void* stream);
 
 /*
- * tf_trellis_workspace_bytes -- bytes of caller workspace tf_trellis_linear_ws
+ * tf_trellis_workspace_bytes -- (the pages have no counterpart) bytes of
+ * caller workspace tf_trellis_linear_ws
  * needs for this shape on the current device (it depends on the device's SM
  * count: 196,608 bytes of partial sums per SM for passes of up to 128 rows,
  * plus 4 bytes per output block), or 0 for an invalid shape or width, or
@@ -171,7 +174,8 @@ tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* 
 
 /*
  * tf_trellis_linear_noalloc -- the same computation as tf_trellis_linear
- * (same arguments, layouts, results and refusals) for callers that must not
+ * (same arguments, layouts and results bit for bit; the same refusals, plus
+ * TF_ERR_SCRATCH above 2,097,152 outputs) for callers that must not
  * let a library allocate device memory: for example a serving process whose
  * caching allocator has already reserved the memory it plans around, where
  * a cudaMalloc can fail or break that plan, or code that cannot accept the
@@ -183,13 +187,15 @@ tf_status tf_trellis_linear_ws(const void* xr, const void* trellis, const void* 
  * exits. Limits: out_features <= 2,097,152 (16,384 blocks of 128), else
  * TF_ERR_SCRATCH; at most 160 thread blocks per launch. The first call on a
  * device looks up the array's device address on that device (call it once
- * before capturing work into a CUDA graph). Each call clears the counters it
- * uses with cudaMemsetAsync on `stream`. All calls share the one array, so
+ * before capturing work into a CUDA graph). Each pass of up to 16 rows first
+ * clears the counters it uses with cudaMemsetAsync on `stream` (so a pass
+ * that gave up a bounded wait leaves nothing stale for the next). All calls
+ * share the one array, so
  * calls whose work overlaps on the GPU (for example on two streams) race and
  * must be ordered by the caller. Calls no cudaMalloc or cudaFree. It runs
  * its passes of up to 16 rows on the mma.sync kernel (whose partial sums fit
  * the array); every output has the same bits as tf_trellis_linear's, which
- * may run the same pass on the tcgen05 kernel.
+ * runs its passes on the tcgen05 kernel.
  */
 tf_status tf_trellis_linear_noalloc(const void* xr, const void* trellis, const void* svh,
                                     void* y, int out_dtype, int rows, int in_features,
@@ -217,20 +223,30 @@ tf_status tf_trellis_decode(const void* trellis, void* w, int in_features,
 tf_status tf_selftest_stranded_wait(void* stream);
 
 /* Bytes of a packed trellis: in_features * out_features * bits / 8, or 0 for
- * an invalid shape or width. */
+ * an invalid shape or width. The size follows from the format of "What this
+ * changes", second bullet: 16 x 16 tiles, each weight one step of a
+ * bits-per-weight trellis, so a tile is 256 * bits bits (the tile layout
+ * above), and in/16 * out/16 tiles make the matrix. */
 size_t tf_trellis_bytes(int in_features, int out_features, int bits);
 
-/* Static text for a status code. */
+/* Static text for a status code. The refusal codes (TF_ERR_SHAPE,
+ * TF_ERR_BITS, TF_ERR_DTYPE, TF_ERR_NULL, TF_ERR_ALIGN) play the part of the
+ * launches' refusals of shapes they do not fit and of unknown widths ("What
+ * this changes", last bullet: the launches with the shapes they refuse); the
+ * others (TF_ERR_CUDA, TF_ERR_TIMEOUT, TF_ERR_POINTER, TF_ERR_SCRATCH) are
+ * this library's own records, with no counterpart on the pages. */
 const char* tf_status_string(int status);
 
-/* Text of the last TF_ERR_CUDA on the calling host thread ("" if none). */
+/* Text of the last TF_ERR_CUDA on the calling host thread ("" if none).
+ * The pages have no counterpart. */
 const char* tf_last_error(void);
 
 /*
  * tf_device_error -- synchronises `stream`, then returns TF_ERR_TIMEOUT if a
  * kernel of this library on the current device gave up a bounded wait since
  * the last call (and clears that record), TF_ERR_CUDA if the synchronisation
- * failed, else TF_OK.
+ * failed, else TF_OK. The pages have no counterpart (their kernels have no
+ * waits that can give up).
  */
 tf_status tf_device_error(void* stream);
 

@@ -83,3 +83,30 @@ def assert_close_bf16(ybits, y_ref, tol=REL_TOL):
     good = err <= slack + half_place
     assert np.all(good), "bf16 output outside bound at %s" % (np.argwhere(~good)[:5].tolist(),)
     return float(np.max(err / rms))
+
+
+def unit_k_tiles(in_features, bits):
+    """k-tiles per unit of work of the linear's launch (16 where the inputs
+    are a multiple of 256 and bits <= 5, else 8)."""
+    return 16 if (in_features % 256 == 0 and bits <= 5) else 8
+
+
+def launch_ctas(num_sms, in_features, out_features, bits):
+    """CTAs of one linear launch: one per SM, at most one per unit."""
+    units = (out_features // 128) * (in_features // (16 * unit_k_tiles(in_features, bits)))
+    return min(units, num_sms)
+
+
+def cut_blocks(num_sms, in_features, out_features, bits):
+    """Output blocks the launch's work split cuts between two or more CTAs
+    (their sums go through the cross-CTA partial-sum path): the (block, unit)
+    grid, block-major, cut into one contiguous range per CTA."""
+    ub = in_features // (16 * unit_k_tiles(in_features, bits))
+    units = (out_features // 128) * ub
+    ctas = launch_ctas(num_sms, in_features, out_features, bits)
+    out = set()
+    for c in range(1, ctas):
+        u = c * units // ctas          # first unit of CTA c
+        if u % ub:
+            out.add(u // ub)
+    return sorted(out)

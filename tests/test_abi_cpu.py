@@ -124,3 +124,31 @@ def test_without_gpu_a_valid_call_fails_cleanly(lib):
         pytest.skip("a GPU is present")
     assert lin(lib) in (tf.TF_ERR_CUDA, tf.TF_ERR_POINTER)
     assert "" != lib.tf_last_error().decode() or True
+
+
+PAGE_SECTIONS = ("What this changes", "Checks on this head", "Kernel contract", "Known limits")
+
+
+def comment_before_each_declaration():
+    """(function name, the comment block right before its declaration) for
+    every function the public headers declare."""
+    out = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        pattern = r"/\*((?:(?!\*/).)*)\*/\s*((?:const\s+)?[a-z_0-9]+\s*\*?\s*)(tf_[a-z0-9_]+)\s*\("
+        for m in re.finditer(pattern, text, re.S):
+            out.append((m.group(3), m.group(1)))
+    return out
+
+
+def test_every_entry_point_cites_a_passage_or_says_it_has_none():
+    """Each declaration's comment names the page section it follows (quoted)
+    or says that the pages have no counterpart."""
+    found = comment_before_each_declaration()
+    assert {n for n, _ in found} == declared_functions()
+    for name, comment in found:
+        flat = " ".join(comment.replace("*", " ").split())
+        cites = any('"%s"' % sec in flat or "%s," % sec in flat for sec in PAGE_SECTIONS)
+        assert cites or "no counterpart" in flat, name

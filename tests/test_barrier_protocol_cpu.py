@@ -95,29 +95,39 @@ def wait(bar, parity):
 # --------------------------------------------------------------------------
 # The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
 
-def run_tc(order, S, WG, H, rng):
+def run_tc(order, S, WG, H, rng, AB=1, ACC=1, plant=None):
+    """The tcgen05 kernel: a weights producer and an xr producer, each
+    refilling its part of a stage once that part's reader is done (the decode
+    warpgroup for the weights, the MMAs for xr); WG decode warpgroups with AB
+    A buffers each; one MMA warp; ACC accumulator sets alternating between
+    segments. `plant` names a fault to plant: "w_early" refills a stage's
+    weights without waiting for the decode, "x_early" refills its xr slice
+    without waiting for the MMAs."""
     sim = Sim(rng)
     n_half = order.n_units * H
-    full = [Bar("full%d" % s, 1) for s in range(S)]
-    empty = [Bar("empty%d" % s, 4 + 1) for s in range(S)]
-    afull = [Bar("afull%d" % w, 4) for w in range(WG)]
-    aempty = [Bar("aempty%d" % w, 1) for w in range(WG)]
-    dfull, dempty = Bar("dfull", 1), Bar("dempty", 4)
-    stage = [None] * S       # half-unit whose copy the stage holds
-    abuf = [None] * WG       # half-unit whose decoded weights the A buffer holds
-    acc = [None]             # segment whose sums the accumulators hold
-    STAGE_BYTES = 3
+    wfull = [Bar("wfull%d" % s, 1) for s in range(S)]
+    wempty = [Bar("wempty%d" % s, 4) for s in range(S)]
+    xfull = [Bar("xfull%d" % s, 1) for s in range(S)]
+    xempty = [Bar("xempty%d" % s, 1) for s in range(S)]
+    afull = [[Bar("afull%d.%d" % (w, b), 4) for b in range(AB)] for w in range(WG)]
+    aempty = [[Bar("aempty%d.%d" % (w, b), 1) for b in range(AB)] for w in range(WG)]
+    dfull = [Bar("dfull%d" % d, 1) for d in range(ACC)]
+    dempty = [Bar("dempty%d" % d, 4) for d in range(ACC)]
+    wtag = [None] * S        # half-unit whose weights a stage holds
+    xtag = [None] * S        # half-unit whose xr slice a stage holds
+    abuf = [[None] * AB for _ in range(WG)]  # half-unit whose decoded weights an A buffer holds
+    acc = [None] * ACC       # segment whose sums an accumulator set holds
 
-    def producer():
+    def producer(full, empty, tag, wait_empty):
         for q in range(n_half):
             s = q % S
-            if q >= S:
+            if q >= S and wait_empty:
                 yield wait(empty[s], ((q // S) - 1) & 1)
-            full[s].arrive_expect_tx(STAGE_BYTES)
+            full[s].arrive_expect_tx(1)
 
             def land(s=s, q=q):
-                stage[s] = q
-                full[s].complete_tx(STAGE_BYTES)
+                tag[s] = q
+                full[s].complete_tx(1)
             sim.copies.append(land)
 
     def decode(wg):
@@ -125,16 +135,17 @@ def run_tc(order, S, WG, H, rng):
         while WG * j + wg < n_half:
             q = WG * j + wg
             s = q % S
-            yield wait(full[s], (q // S) & 1)
-            if j >= 1:
-                yield wait(aempty[wg], (j - 1) & 1)
-            assert stage[s] == q, "decode of %d read stage %d holding %s" % (q, s, stage[s])
-            abuf[wg] = q
+            ab = j % AB
+            yield wait(wfull[s], (q // S) & 1)
+            if j >= AB:
+                yield wait(aempty[wg][ab], ((j // AB) - 1) & 1)
+            assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
+            abuf[wg][ab] = q
             yield None                                    # the decode takes a while
-            assert stage[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
+            assert wtag[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
             for _ in range(4):
-                afull[wg].arrive()
-                empty[s].arrive()
+                wempty[s].arrive()
+                afull[wg][ab].arrive()
             j += 1
 
     def mma():
@@ -142,40 +153,45 @@ def run_tc(order, S, WG, H, rng):
             bb = order.block(sg)
             seg_lo, seg_hi = order.lo(bb), order.hi(bb)
             base = order.pos(sg, seg_lo) - seg_lo
-            if sg >= 1:
-                yield wait(dempty, (sg - 1) & 1)
+            d = sg % ACC
+            if sg >= ACC:
+                yield wait(dempty[d], ((sg // ACC) - 1) & 1)
             for i in range(seg_lo, seg_hi):
                 for h in range(H):
                     q = (base + i) * H + h
                     s, wg, j = q % S, q % WG, q // WG
-                    yield wait(full[s], (q // S) & 1)
-                    yield wait(afull[wg], j & 1)
+                    ab = j % AB
+                    yield wait(xfull[s], (q // S) & 1)
+                    yield wait(afull[wg][ab], (j // AB) & 1)
 
-                    def execute(q=q, s=s, wg=wg, sg=sg):
-                        assert stage[s] == q, "MMA of %d found stage %d holding %s" % (q, s, stage[s])
-                        assert abuf[wg] == q, "MMA of %d found A buffer %d holding %s" % (q, wg, abuf[wg])
-                        acc[0] = sg
-                        aempty[wg].arrive()                  # the two commits after the MMAs
-                        empty[s].arrive()
+                    def execute(q=q, s=s, wg=wg, ab=ab, sg=sg, d=d):
+                        assert xtag[s] == q, "MMA of %d found stage %d's xr of %s" % (q, s, xtag[s])
+                        assert abuf[wg][ab] == q, "MMA of %d found A buffer %d.%d holding %s" % (
+                            q, wg, ab, abuf[wg][ab])
+                        acc[d] = sg
+                        aempty[wg][ab].arrive()              # the two commits after the MMAs
+                        xempty[s].arrive()
                     sim.tensor.append(execute)
-            sim.tensor.append(dfull.arrive)                  # commit at the segment's end
+            sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
 
     def epilogue():
         for sg in range(order.n_seg):
-            yield wait(dfull, sg & 1)
-            assert acc[0] == sg, "segment %d read accumulators of %s" % (sg, acc[0])
+            d = sg % ACC
+            yield wait(dfull[d], (sg // ACC) & 1)
+            assert acc[d] == sg, "segment %d read accumulators of %s" % (sg, acc[d])
             yield None                                    # the readout takes a while
-            assert acc[0] == sg, "accumulators of segment %d overwritten during readout" % sg
+            assert acc[d] == sg, "accumulators of segment %d overwritten during readout" % sg
             for _ in range(4):
-                dempty.arrive()
+                dempty[d].arrive()
 
-    sim.add(producer())
+    sim.add(producer(wfull, wempty, wtag, plant != "w_early"))
+    sim.add(producer(xfull, xempty, xtag, plant != "x_early"))
     for wg in range(WG):
         sim.add(decode(wg))
     sim.add(mma())
     sim.add(epilogue())
     sim.run()
-    assert all(stage[s] is not None for s in range(min(S, n_half)))
+    assert all(wtag[s] is not None for s in range(min(S, n_half)))
 
 
 # --------------------------------------------------------------------------
@@ -256,12 +272,28 @@ def cta_orders(seed, n):
         yield SegmentOrder(u0, u1, ub)
 
 
-@pytest.mark.parametrize("S,WG,H", [(12, 3, 2), (9, 3, 2), (6, 3, 1), (4, 4, 2), (8, 4, 1)])
-def test_tc_kernel_protocol_under_random_schedules(S, WG, H):
-    rng = random.Random(100 * S + 10 * WG + H)
+@pytest.mark.parametrize("S,WG,H,AB,ACC", [(18, 3, 2, 2, 2), (12, 3, 2, 2, 2), (9, 3, 2, 2, 1), (6, 3, 1, 2, 2),
+                                            (4, 4, 2, 1, 1), (8, 4, 1, 1, 1), (12, 3, 2, 1, 1)])
+def test_tc_kernel_protocol_under_random_schedules(S, WG, H, AB, ACC):
+    rng = random.Random(100 * S + 10 * WG + H + 1000 * AB + 10000 * ACC)
     for order in cta_orders(S * WG + H, 60):
         for _ in range(3):
-            run_tc(order, S, WG, H, rng)
+            run_tc(order, S, WG, H, rng, AB, ACC)
+
+
+@pytest.mark.parametrize("plant", ["w_early", "x_early"])
+def test_tc_planted_early_refills_are_caught(plant):
+    """A producer that refills its part of a stage without waiting for that
+    part's reader must fail some schedule."""
+    rng = random.Random(21)
+    failures = 0
+    for order in cta_orders(21, 40):
+        for _ in range(5):
+            try:
+                run_tc(order, 6, 3, 2, rng, 2, 2, plant=plant)
+            except AssertionError:
+                failures += 1
+    assert failures > 0
 
 
 @pytest.mark.parametrize("S", [4, 6, 8, 12])
@@ -274,12 +306,13 @@ def test_mma_kernel_protocol_under_random_schedules(S):
 
 def test_planted_fault_is_caught():
     """Stages that are not a multiple of the consumers: a stage's previous
-    half-unit went to another warpgroup, which can still be reading it when
-    its new copy is ordered, and a parity wait can pass on the wrong phase.
-    Some schedule must fail."""
+    half-unit went to another warpgroup, so a warpgroup can wait for a
+    stage's next copy before its previous one has landed, and the parity
+    wait passes on the wrong phase. Some schedule must fail (about one in
+    two hundred does, so many are run)."""
     rng = random.Random(7)
     failures = 0
-    for order in cta_orders(7, 40):
+    for order in cta_orders(7, 400):
         for _ in range(5):
             try:
                 run_tc(order, 5, 4, 2, rng)

@@ -106,7 +106,7 @@ def tc_stages(bits, slots, budget=227 * KIB):
     wg = 3 if slots <= 64 else 4
     stage = 256 * bits * 8 + slots * 16 * 8 * 2
     fit = (budget - 8192 - 2048) // stage
-    return (min(fit, 12) // wg) * wg, wg
+    return (min(fit, 18) // wg) * wg, wg
 
 
 def ranges(units, ctas):
@@ -163,7 +163,7 @@ def test_stage_counts_keep_each_stage_with_one_consumer(bits):
     for ukt in ([16, 8] if bits <= 5 else [8]):
         s = mma_stages(bits, ukt)
         assert s >= 4 and s % 2 == 0, (bits, ukt, s)       # two groups, two stages each at least
-    for slots in (32, 64, 128):
+    for slots in (16, 32, 64, 128):
         s, wg = tc_stages(bits, slots)
         assert s >= wg and s % wg == 0, (bits, slots, s)
         # Half-unit q is decoded by warpgroup q % wg from stage q % s, so the
@@ -175,6 +175,7 @@ def test_stage_counts_keep_each_stage_with_one_consumer(bits):
 def test_stage_counts_of_the_measured_classes():
     """The counts the measurements were taken with (4 bits)."""
     assert mma_stages(4, 16) == 6
+    assert tc_stages(4, 16) == (18, 3)
     assert tc_stages(4, 32) == (12, 3)
     assert tc_stages(4, 64) == (9, 3)
     assert tc_stages(4, 128) == (4, 4)

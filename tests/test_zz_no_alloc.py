@@ -30,7 +30,8 @@ def _call_noalloc(xr_t, tr_t, svh_t, y_t, bits, rows, i_f, o_f):
     return lib.tf_trellis_linear_noalloc(
         ctypes.c_void_p(xr_t.data_ptr()), ctypes.c_void_p(tr_t.data_ptr()),
         ctypes.c_void_p(svh_t.data_ptr()), ctypes.c_void_p(y_t.data_ptr()),
-        tf.TF_F32 if y_t.dtype == torch.float32 else tf.TF_F16, rows, i_f, o_f, bits,
+        {torch.float32: tf.TF_F32, torch.float16: tf.TF_F16, torch.bfloat16: tf.TF_BF16}[y_t.dtype],
+        rows, i_f, o_f, bits,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -81,8 +82,36 @@ def test_noalloc_mma_kernel_bit_equal_to_tcgen05_kernel(bits):
         assert np.array_equal(got, want), "bits %d, %d rows: the two kernels differ" % (bits, rows)
 
 
+@pytest.mark.parametrize("rows,out_dtype", [(64, "f32"), (5, "bf16"), (33, "bf16")])
+def test_noalloc_many_passes_and_bf16_bit_equal(rows, out_dtype):
+    """Several 16-row passes in one call (each pass clears the counters it
+    uses and writes its own rows of y) and the bf16 store path: the same bits
+    as tf_trellis_linear, on two calls in a row."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    i_f, o_f, bits = 2048, 8192, 4
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16}[out_dtype]
+    tr_t = dev(synth.make_trellis(i_f, o_f, bits, 960))
+    svh_t = dev(synth.make_scale(o_f, 961))
+    xr_t = tf.tf_rot_in(dev(synth.make_x(rows, i_f, 962)), dev(synth.make_scale(i_f, 963)))
+    want = host(tf.tf_trellis_linear(xr_t, tr_t, svh_t, bits, o_f, out_dtype=dt))
+    for _ in range(2):
+        y_t = torch.full((rows, o_f), float("nan"), dtype=dt, device="cuda")
+        assert _call_noalloc(xr_t, tr_t, svh_t, y_t, bits, rows, i_f, o_f) == tf.TF_OK
+        tf.tf_device_error()
+        got = host(y_t)
+        assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), "rows %d %s" % (rows, out_dtype)
+
+
 def test_noalloc_refuses_more_outputs_than_its_array_holds():
+    """Shapes tf_trellis_linear refuses get its status; shapes it accepts but
+    the fixed array cannot hold get TF_ERR_SCRATCH."""
     lib = tf.lib()
     p = ctypes.c_void_p(0x10000)
-    st = lib.tf_trellis_linear_noalloc(p, p, p, p, tf.TF_F32, 1, 512, 128 * 20000, 4, ctypes.c_void_p(0))
-    assert st == tf.TF_ERR_SCRATCH
+    s0 = ctypes.c_void_p(0)
+    f = lib.tf_trellis_linear_noalloc
+    assert f(p, p, p, p, tf.TF_F32, 1, 512, 128 * 20000, 4, s0) == tf.TF_ERR_SCRATCH
+    assert f(p, p, p, p, tf.TF_F32, 1, 512, 2097152 + 128, 4, s0) == tf.TF_ERR_SCRATCH
+    assert f(p, p, p, p, tf.TF_F32, 1, 512, (1 << 24) + 128, 4, s0) == tf.TF_ERR_SHAPE
+    assert f(p, p, p, p, tf.TF_F32, 1, 512, 100, 4, s0) == tf.TF_ERR_SHAPE
+    assert f(p, p, p, p, tf.TF_F32, 1, 512, 128, 7, s0) == tf.TF_ERR_BITS

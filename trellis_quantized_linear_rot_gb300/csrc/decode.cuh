@@ -161,30 +161,6 @@ __device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWor
   }
 }
 
-// The same words from a tile whose consecutive words sit STRIDE words apart
-// (the strips order interleaves the words of four k-tiles).
-template <int BITS, int STRIDE>
-__device__ __forceinline__ void load_col_words_strided(const uint32_t* tw, int n, ColWords<BITS>& cw) {
-  if constexpr (BITS == 4) {
-    cw.w[0] = tw[((2 * n + 31) & 31) * STRIDE];
-    cw.w[1] = tw[(2 * n) * STRIDE];
-    cw.w[2] = tw[(2 * n + 1) * STRIDE];
-  } else if constexpr (BITS == 8) {
-    cw.w[0] = tw[((4 * n + 63) & 63) * STRIDE];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cw.w[1 + j] = tw[(4 * n + j) * STRIDE];
-  } else {
-    using S = RowSpan<BITS>;
-    const int w0 = row_first_bit<BITS>(n) >> 5;
-#pragma unroll
-    for (int j = 0; j < S::kWords; ++j) {
-      int wi = w0 + j;
-      wi = (wi >= S::kTileWords) ? wi - S::kTileWords : wi;
-      cw.w[j] = tw[wi * STRIDE];
-    }
-  }
-}
-
 template <int BITS>
 __device__ __forceinline__ void decode_col_words(const ColWords<BITS>& cw, int n, uint32_t (&out)[8]) {
   if constexpr (BITS == 4) {
@@ -335,42 +311,6 @@ __device__ __forceinline__ void decode_group4_words(const Group4Words<BITS>& gw,
   } else {
     const uint32_t a0 = __funnelshift_l(gw.x[1], gw.x[0], off);
     const uint32_t a1 = __funnelshift_l(gw.x[2], gw.x[1], off);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] = __funnelshift_l(a1, a0, j * BITS) >> 16;
-  }
-  lo = mul1_pair(mul1_half_plus_1024(s[0]), mul1_half_plus_1024(s[1]));
-  hi = mul1_pair(mul1_half_plus_1024(s[2]), mul1_half_plus_1024(s[3]));
-}
-
-// Packs weights (4t, 4t+1) and (4t+2, 4t+3) of output n as two half2 words.
-template <int BITS>
-__device__ __forceinline__ void decode_group4(const uint32_t* tw, int n, int t, uint32_t& lo, uint32_t& hi) {
-  using G = Group4<BITS>;
-  const int start = ((16 * n + 4 * t) * BITS + BITS - 16 + G::kTileBits) % G::kTileBits;
-  const int w0 = start >> 5;
-  const int off = start & 31;
-  uint32_t s[4];
-  if constexpr (G::kWords == 2) {
-    const int w1 = (w0 + 1 == G::kTileWords) ? 0 : w0 + 1;
-    const uint32_t x0 = tw[w0];
-    const uint32_t x1 = tw[w1];
-    const uint32_t p = __funnelshift_l(x1, x0, off);  // the group's bits, first window at the top
-    if constexpr (BITS == 4) {
-      const uint32_t p4 = p >> 4;
-      s[0] = hi16(p);
-      s[1] = mid16(p4);
-      s[2] = mid16(p);
-      s[3] = lo16(p4);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) s[j] = (p >> (16 - j * BITS)) & 0xFFFFu;
-    }
-  } else {
-    const int w1 = (w0 + 1 == G::kTileWords) ? 0 : w0 + 1;
-    const int w2 = (w1 + 1 == G::kTileWords) ? 0 : w1 + 1;
-    const uint32_t x0 = tw[w0], x1 = tw[w1], x2 = tw[w2];
-    const uint32_t a0 = __funnelshift_l(x1, x0, off);
-    const uint32_t a1 = __funnelshift_l(x2, x1, off);
 #pragma unroll
     for (int j = 0; j < 4; ++j) s[j] = __funnelshift_l(a1, a0, j * BITS) >> 16;
   }

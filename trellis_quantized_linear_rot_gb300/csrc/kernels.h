@@ -33,15 +33,15 @@ constexpr size_t kTcPartialFloatsPerCta = 3 * 128 * 128;
 constexpr size_t kMmaPartialFloatsPerCta = 2 * 16 * 128;
 constexpr size_t kPartialFloatsPerCta = kTcPartialFloatsPerCta;
 
-// The kernel of a pass, as measured on the GB300 (LM head and wkv shapes):
-// the mma.sync kernel is faster for passes of up to 8 rows at 2 to 5 bits in
-// the strips order; the tcgen05 kernel everywhere else (up to 18 % at 6 and
-// 8 bits, and in the k-tile order). A workspace too small for the tcgen05
-// kernel's partial sums keeps passes of up to 16 rows on the mma.sync one.
+// The kernel of a pass: the tcgen05 kernel wherever the workspace holds its
+// partial sums; a workspace too small for them (the no-allocation entry
+// point's) keeps passes of up to 16 rows on the mma.sync kernel. Both give
+// every row the same bits.
 inline bool pass_uses_tc(int rows, int bits, bool strips, size_t partial_floats_per_cta) {
+  (void)bits;
+  (void)strips;
   if (rows > kMaxDecodePassRows) return true;
-  if (partial_floats_per_cta < kTcPartialFloatsPerCta) return false;
-  return !(strips && bits <= 5 && rows <= 8);
+  return partial_floats_per_cta >= kTcPartialFloatsPerCta;
 }
 
 // One pass of at most kMaxPassRows rows through the trellis linear.

@@ -51,6 +51,7 @@
 #include "decode.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "per_device.h"
 #include "ptx.cuh"
 
 namespace tfx {
@@ -553,15 +554,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+constexpr int kMaxAttrDevices = 64;
+
+// The dynamic shared-memory limit of a kernel, set once on each device that
+// launches it (the attribute belongs to the current device).
+template <typename Kernel>
+cudaError_t smem_attr_once(PerDeviceOnce<kMaxAttrDevices>& once, Kernel kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return static_cast<cudaError_t>(once.run(dev, static_cast<int>(cudaErrorInvalidDevice), [&] {
+    return static_cast<int>(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  }));
+}
+
 template <int BITS, int NB, int LAYOUT, int UKT>
 cudaError_t set_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(trellis_linear_mma_kernel<BITS, NB, LAYOUT, UKT>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS, UKT, NB>::kBytes);
-  });
-  return err;
+  static PerDeviceOnce<kMaxAttrDevices> once;
+  return smem_attr_once(once, trellis_linear_mma_kernel<BITS, NB, LAYOUT, UKT>, Layout<BITS, UKT, NB>::kBytes);
 }
 
 template <int BITS, int NB, int LAYOUT, int UKT>

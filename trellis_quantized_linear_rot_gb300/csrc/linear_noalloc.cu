@@ -51,8 +51,9 @@ using namespace tfx;
 extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trellis, const void* svh,
                                                void* y, int out_dtype, int rows, int in_features,
                                                int out_features, int bits, void* stream) {
+  // The refusals of tf_trellis_linear first, then the limit of the array.
   if (rows < 0 || in_features <= 0 || in_features % 128 || in_features > (1 << 20) ||
-      out_features <= 0 || out_features % 128)
+      out_features <= 0 || out_features % 128 || out_features > (1 << 24))
     return TF_ERR_SHAPE;
   if (!(bits == 2 || bits == 3 || bits == 4 || bits == 5 || bits == 6 || bits == 8)) return TF_ERR_BITS;
   if (out_dtype != TF_F16 && out_dtype != TF_F32 && out_dtype != TF_BF16) return TF_ERR_DTYPE;
@@ -90,12 +91,14 @@ extern "C" tf_status tf_trellis_linear_noalloc(const void* xr, const void* trell
   ws.ctas = trellis_linear_mma_ctas(num_sms < kNoAllocMaxCtas ? num_sms : kNoAllocMaxCtas, in_features,
                                     out_features, bits);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The counters must start at zero; a completed launch leaves them at zero,
-  // but clear the ones this call uses in case an earlier launch was cut short.
-  cudaError_t e = cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(out_features / 128) * sizeof(int), st);
-  if (e != cudaSuccess) return record_cuda_error(e, "cudaMemsetAsync (no-alloc counters)");
   const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
   for (int r0 = 0; r0 < rows; r0 += 16) {
+    // The counters must start at zero. A completed launch leaves them at
+    // zero, but one that gave up a bounded wait may not, so every pass
+    // clears the ones it uses first.
+    cudaError_t e =
+        cudaMemsetAsync(ws.counters, 0, static_cast<size_t>(out_features / 128) * sizeof(int), st);
+    if (e != cudaSuccess) return record_cuda_error(e, "cudaMemsetAsync (no-alloc counters)");
     LinearPass p;
     p.xr = static_cast<const __half*>(xr) + static_cast<size_t>(r0) * in_features;
     p.trellis = static_cast<const uint32_t*>(trellis);

@@ -1,41 +1,59 @@
-// The trellis linear for passes of up to 128 rows on GB300 (prompts, and the
-// decode passes the mma.sync kernel is slower at):
-// tcgen05 MMAs with the decoded weights in Tensor Memory, the same results
-// bit for bit as the decode-row kernel (linear_mma.cuh).
+// The trellis linear on GB300 with tcgen05: the decoded weights go to
+// Tensor Memory and tensor-core MMAs form the K sums of every pass, from one
+// decode row up to 128 rows, with the same results bit for bit as the
+// mma.sync kernel (linear_mma.cuh).
 //
 // Method: "hip exl3: the input rotation and trellis linear for decode rows",
-// section "Known limits": the prompt path follows, registered bit-equal to
-// the decode linear. Bit-equality holds because every output element goes
-// through the same sums as in the decode-row kernel: the same cut of the
-// (block, unit) grid between CTAs, the same two chains per segment (the units
-// at even and at odd processing positions, each a chain of K = 16 tensor-core
-// steps in input order), their fp32 sum in that order, and the partial sums
-// of a shared block added in CTA order. A tcgen05.mma (M = 128, K = 16, A in
-// Tensor Memory) gives the same bits as mma.sync.m16n8k16 for the same
-// operands and accumulator, also when the 16 inputs of a step are presented
-// in another order (checked on the GB300 over 81,920 outputs of chains of
-// eight steps with wide exponent ranges).
+// section "What this changes" (second bullet: the trellis linear for 1 to 16
+// rows a pass, a row's sums in a fixed order that does not depend on the
+// rows sharing its launch) and section "Known limits" (the prompt path,
+// registered bit-equal to the decode linear). Bit-equality holds because
+// every output element goes through the same sums in every pass and in both
+// kernels: the same cut of the (block, unit) grid between CTAs, the same two
+// chains per segment (the units at even and at odd processing positions,
+// each a chain of K = 16 tensor-core steps in input order), their fp32 sum
+// in that order, and the partial sums of a shared block added in CTA order.
+// A tcgen05.mma (M = 128, K = 16, A in Tensor Memory) gives the same bits as
+// mma.sync.m16n8k16 for the same operands and accumulator, also when the 16
+// inputs of a step are presented in another order (checked on the GB300 over
+// 81,920 outputs of chains of eight steps with wide exponent ranges).
 //
 // Per CTA (one per SM): the MMA's M is the 128 outputs of a block (Tensor
-// Memory lanes), N the pass's row slots (rows rounded up to 16, at most 128),
-// K 16 inputs per k-tile.
+// Memory lanes), N the pass's row slots (rows rounded up to 16), K 16 inputs
+// per k-tile.
+//
 // Warp roles:
 //   warps 0-3   epilogue: per segment, the two chains' sums from Tensor
 //               Memory, added, written to this CTA's partial-sum slot, then
 //               (when the CTA owns the block, or arrives last) the output
 //               rotation, svh and the stores
-//   warps 4-15  decode: three warpgroups (passes of up to 64 row slots;
-//               warps 4-19, four warpgroups, at 128) take half-units (8
-//               k-tiles) in turn;
-//               thread n decodes output n's 16 weights of each k-tile into
-//               Tensor Memory lane n (the MMA's A operand)
-//   next warp   producer: the copies of each half-unit into a ring of
-//               stages sized by the pass's row-slot class (packed weights, and
-//               the xr slice of the pass's row slots: two tensor copies of
-//               64 inputs x N rows with the 128-byte swizzle, which is the
-//               MMA's K-major B layout)
+//   warps 4-    decode: three warpgroups (four at 128 row slots) take
+//               half-units (8 k-tiles) in turn; thread n decodes output n's
+//               16 weights of each k-tile into Tensor Memory lane n (the MMA's
+//               A operand), in one of its warpgroup's A buffers
+//   next warp   weights producer: one thread copies each half-unit's packed
+//               weights into the stage ring as soon as the decode of the
+//               stage's previous half-unit is done
+//   next warp   xr producer: one thread copies each half-unit's xr slice
+//               (two tensor copies of 64 inputs x the pass's row slots, with
+//               the 128-byte swizzle: the MMA's K-major B layout) as soon as
+//               the MMAs of the stage's previous half-unit are done
 //   last warp   MMA: allocates Tensor Memory; the warp runs the MMA loop and
 //               one elected lane issues
+// A stage holds a half-unit's weights and its xr slice, each part with its
+// own full and empty barriers: the weights are read by the decode and the
+// xr slice by the MMAs, so each part is refilled as soon as its reader is
+// done, by its own thread. A single thread issuing every copy was the
+// kernel's bottleneck (measured on the GB300: a thread issuing 1-D bulk
+// copies alone manages one copy per ~500 cycles whatever its size, most of it
+// the thread's own chain of dependent instructions), so the two producers
+// keep their loops short and work from counters, not divisions.
+//
+// Ordering with the kernel before this one (programmatic dependent launch):
+// every thread that reads memory that kernel may write (xr, by the xr
+// producer's copies) or touches the partial sums, counters or y (the
+// epilogue) first executes griddepcontrol.wait; the weight copies and the
+// decode may run before it.
 // All waits are bounded; a kernel that gives up sets the error flag and exits.
 #pragma once
 
@@ -45,37 +63,49 @@ namespace tfx {
 
 namespace {
 
-constexpr int kTcRows = 128;     // row slots of a pass (the MMA's N)
-constexpr int kTcHalfKt = 8;     // k-tiles per staged half-unit
-constexpr int kTcTmemCols = 512;  // acc[2] at columns 0 and 128; one A buffer per warpgroup at 256 + 64 wg
+constexpr int kTcRows = 128;        // row slots of the largest pass (the MMA's N)
+constexpr int kTcHalfKt = 8;        // k-tiles per staged half-unit
+constexpr int kTcTmemCols = 512;    // accumulators, then the decode warpgroups' A buffers
 constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared block
 
-// Shared memory of a pass class: stages of a half-unit's packed weights and
-// its xr slice for up to SLOTS row slots (32, 64 or 128). Fewer slots make
-// smaller stages and so more of them in flight: 12 / 9 / 4 at 4 bits (the
-// copies of a stage take longer to land than a warpgroup takes to decode
-// one half-unit, so a warpgroup needs stages beyond the one it decodes).
+// Shared memory and Tensor Memory of a pass class (SLOTS = 16, 32, 64 or 128
+// row slots): a stage holds a half-unit's packed weights and its xr slice for
+// SLOTS row slots, so fewer slots make smaller stages and more of them (18 /
+// 12 / 9 / 4 at 4 bits).
 template <int BITS, int SLOTS>
 struct TcCfg {
   static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
-  static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // up to SLOTS rows x 128 inputs, fp16
+  static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // SLOTS rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
+  // Decode warpgroups: three up to 64 row slots, four at 128 (measured at 4
+  // and 6 bits).
+  static constexpr int kWG = SLOTS <= 64 ? 3 : 4;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
   // to the same decode warpgroup.
-  // Decode warpgroups: three up to 64 row slots, where the decode warps
-  // mostly wait and fewer of them leave the MMA and producer warps more issue
-  // slots and more stages fit; four at 128 slots (measured at 4 and 6 bits).
-  static constexpr int kWG = SLOTS <= 64 ? 3 : 4;
-  static constexpr int kProducer = 4 + 4 * kWG;  // warp roles: epilogue 0-3, decode, producer, MMA
-  static constexpr int kMma = kProducer + 1;
+  static constexpr int kStages = (kStagesFit < 18 ? kStagesFit : 18) / kWG * kWG;
+  // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
+  // in kAccBufs sets that alternate between segments (so that the MMAs of a
+  // segment can start while the epilogue reads the previous one), then
+  // kABufs A buffers of 64 columns (8 k-tiles) per decode warpgroup (so that
+  // a warpgroup decodes its next half-unit while the MMAs read its last).
+  static constexpr int kAccBufs = SLOTS <= 32 ? 2 : 1;
+  static constexpr int kABufs = SLOTS <= 64 ? 2 : 1;
+  static constexpr int kACol0 = kAccBufs * 2 * SLOTS;
+  static_assert(kACol0 + kWG * kABufs * 64 <= kTcTmemCols, "Tensor Memory columns");
+  // Warp roles: epilogue 0-3, decode, weights producer, xr producer, MMA.
+  static constexpr int kProdW = 4 + 4 * kWG;
+  static constexpr int kProdX = kProdW + 1;
+  static constexpr int kMma = kProdX + 1;
   static constexpr int kThreads = (kMma + 1) * 32;
-  static constexpr int kStages = (kStagesFit < 12 ? kStagesFit : 12) / kWG * kWG;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
-  static constexpr int kNumBars = 2 * kStages + 2 * kWG + 3;  // full, empty, afull, aempty, dfull, dempty, drain
+  // wfull, wempty, xfull, xempty per stage; afull, aempty per A buffer;
+  // dfull, dempty per accumulator set; drain
+  static constexpr int kNumBars = 4 * kStages + 2 * kWG * kABufs + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
+  static_assert(kBytes <= kSmemBudgetWide, "shared memory");
 };
 
 // Decodes k-tile KK of four (strips order) into Tensor Memory at `a_addr`.
@@ -92,6 +122,20 @@ __device__ __forceinline__ void tc_decode_kt(const ColQuads<BITS>& cq, int col, 
 // `rows` read zeros.
 __host__ __device__ constexpr int tc_row_slots(int rows) { return (rows + 15) & ~15; }
 
+// A ring position: stage index and the parity of its current phase, advanced
+// one half-unit at a time without divisions.
+template <int S>
+struct RingPos {
+  int s = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++s == S) {
+      s = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
 __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -99,23 +143,28 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
   using T = TcCfg<BITS, SLOTS>;
   constexpr int S = T::kStages;
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
-  constexpr int kTcWG = T::kWG;
-  constexpr int kTcProducer = T::kProducer;
-  constexpr int kTcMma = T::kMma;
-  static_assert(S >= kTcWG && S % kTcWG == 0, "stages must stay with one decode warpgroup");
+  constexpr int kWG = T::kWG;
+  constexpr int kAB = T::kABufs;
+  constexpr int kAccB = T::kAccBufs;
+  static_assert(S >= kWG && S % kWG == 0, "stages must stay with one decode warpgroup");
   extern __shared__ __align__(1024) uint8_t smem[];
   float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + T::kXchOff);
   const uint32_t bar0 = smem_u32(smem + T::kBarOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + T::kMiscOff + 8);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  auto afull_bar = [&](int w) { return bar0 + 8u * (2 * S + w); };
-  auto aempty_bar = [&](int w) { return bar0 + 8u * (2 * S + kTcWG + w); };
-  const uint32_t dfull = bar0 + 8u * (2 * S + 2 * kTcWG);
-  const uint32_t dempty = bar0 + 8u * (2 * S + 2 * kTcWG + 1);
-  const uint32_t drain = bar0 + 8u * (2 * S + 2 * kTcWG + 2);
+  auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+  auto wempty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto xempty_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  const uint32_t abar0 = bar0 + 8u * (4 * S);
+  // A buffer b of warpgroup w; accumulator set d.
+  auto afull_bar = [&](int w, int b) { return abar0 + 8u * (w * kAB + b); };
+  auto aempty_bar = [&](int w, int b) { return abar0 + 8u * (kWG * kAB + w * kAB + b); };
+  const uint32_t dbar0 = abar0 + 8u * (2 * kWG * kAB);
+  auto dfull_bar = [&](int d) { return dbar0 + 8u * d; };
+  auto dempty_bar = [&](int d) { return dbar0 + 8u * (kAccB + d); };
+  const uint32_t drain = dbar0 + 8u * (2 * kAccB);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -132,75 +181,114 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     *abort_flag = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
     *last_flag = 0;
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 4 + 1);  // the decoding warpgroup's 4 warps and the MMA thread
+      mbar_init(wfull_bar(s), 1);
+      mbar_init(wempty_bar(s), 4);  // the decoding warpgroup's 4 warps
+      mbar_init(xfull_bar(s), 1);
+      mbar_init(xempty_bar(s), 1);  // the MMAs' commit
     }
-    for (int w = 0; w < kTcWG; ++w) {
-      mbar_init(afull_bar(w), 4);
-      mbar_init(aempty_bar(w), 1);
+    for (int w = 0; w < kWG; ++w)
+      for (int b = 0; b < kAB; ++b) {
+        mbar_init(afull_bar(w, b), 4);
+        mbar_init(aempty_bar(w, b), 1);
+      }
+    for (int d = 0; d < kAccB; ++d) {
+      mbar_init(dfull_bar(d), 1);
+      mbar_init(dempty_bar(d), 4);
     }
-    mbar_init(dfull, 1);
-    mbar_init(dempty, 4);
     mbar_init(drain, 1);
     fence_barrier_init();
   }
-  if (warp == kTcMma) {
+  if (warp == T::kMma) {
     tmem_alloc(smem_u32(tmem_holder), kTcTmemCols);
     tmem_relinquish();
   }
-  if (warp == kTcProducer && lane == 0) {
-    if (LAYOUT == kLayoutTiles) tma_prefetch_desc(&wmap);
-    tma_prefetch_desc(&xmap);
-  }
+  if (warp == T::kProdW && lane == 0 && LAYOUT == kLayoutTiles) tma_prefetch_desc(&wmap);
+  if (warp == T::kProdX && lane == 0) tma_prefetch_desc(&xmap);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == kTcProducer) {
-    // ------------------------------------------------------------ producer
+  if (warp == T::kProdW) {
+    // ---------------------------------------------------- weights producer
+    // The weights are not written by the kernel before this one, so their
+    // copies start at once.
     if (lane == 0) {
-      pdl_wait_prerequisites();
       UnitCursor cur(order);
+      RingPos<S> rp;
+      int h = 0;
+      const uint8_t* unit_src = p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT);
+      int kt0 = cur.ub() * UKT;
       int issued = 0;
       for (int q = 0; q < n_half; ++q) {
-        const int s = q % S;
-        // A plain wait: the refill of a stage is on the decode warps' path.
-        if (q >= S && !mbar_wait(empty_bar(s), ((q / S) - 1) & 1, abort_flag)) break;
-        const int h = q % H;
-        const int kt0 = cur.ub() * UKT + h * kTcHalfKt;  // first k-tile of the half-unit
-        const uint32_t st = smem_u32(smem + s * T::kStageBytes);
-        mbar_arrive_expect_tx(full_bar(s), T::kWBytes + 2 * xr_box_bytes);
+        if (q >= S && !mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
+        const uint32_t st = smem_u32(smem + rp.s * T::kStageBytes);
+        mbar_arrive_expect_tx(wfull_bar(rp.s), T::kWBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, kt0, full_bar(s));
+          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, kt0 + h * kTcHalfKt, wfull_bar(rp.s));
         else
-          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h * T::kWBytes,
-                       T::kWBytes, full_bar(s));
-        tma_load_2d(st + T::kWBytes, &xmap, kt0 * 16, 0, full_bar(s));
-        tma_load_2d(st + T::kWBytes + xr_box_bytes, &xmap, kt0 * 16 + 64, 0, full_bar(s));
+          bulk_load_1d(st, unit_src + h * T::kWBytes, T::kWBytes, wfull_bar(rp.s));
         issued = q + 1;
-        if (h == H - 1) cur.next();
+        rp.next();
+        if (++h == H) {
+          h = 0;
+          cur.next();
+          unit_src = p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT);
+          kt0 = cur.ub() * UKT;
+        }
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      for (int q = issued - S > 0 ? issued - S : 0; q < issued; ++q) {
+        volatile int never = 0;
+        mbar_wait(wfull_bar(q % S), (q / S) & 1, &never);
+      }
+    }
+  } else if (warp == T::kProdX) {
+    // --------------------------------------------------------- xr producer
+    if (lane == 0) {
+      pdl_wait_prerequisites();  // xr is written by the kernel before this one
+      UnitCursor cur(order);
+      RingPos<S> rp;
+      int h = 0;
+      int x0 = cur.ub() * UKT * 16;  // first input of the unit
+      int issued = 0;
+      for (int q = 0; q < n_half; ++q) {
+        if (q >= S && !mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
+        const uint32_t st = smem_u32(smem + rp.s * T::kStageBytes) + T::kWBytes;
+        const int xi = x0 + h * kTcHalfKt * 16;
+        mbar_arrive_expect_tx(xfull_bar(rp.s), 2 * xr_box_bytes);
+        tma_load_2d(st, &xmap, xi, 0, xfull_bar(rp.s));
+        tma_load_2d(st + xr_box_bytes, &xmap, xi + 64, 0, xfull_bar(rp.s));
+        issued = q + 1;
+        rp.next();
+        if (++h == H) {
+          h = 0;
+          cur.next();
+          x0 = cur.ub() * UKT * 16;
+        }
       }
       for (int q = issued - S > 0 ? issued - S : 0; q < issued; ++q) {
         volatile int never = 0;
-        mbar_wait(full_bar(q % S), (q / S) & 1, &never);
+        mbar_wait(xfull_bar(q % S), (q / S) & 1, &never);
       }
     }
-  } else if (warp >= 4 && warp < kTcProducer) {
+  } else if (warp >= 4 && warp < T::kProdW) {
     // -------------------------------------------------------------- decode
-    const int wg = (warp - 4) >> 2;           // takes half-units wg, wg + kTcWG, ...
+    const int wg = (warp - 4) >> 2;              // takes half-units wg, wg + kWG, ...
     const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
     const int tile = n >> 4, col = n & 15;
+    int s = wg;
+    uint32_t sphase = 0;
     for (int j = 0;; ++j) {
-      const int q = kTcWG * j + wg;
+      const int q = kWG * j + wg;
       if (q >= n_half) break;
-      const int s = q % S;
-      bool ok = mbar_wait(full_bar(s), (q / S) & 1, abort_flag);
-      if (ok && j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
+      const int ab = kAB == 2 ? (j & 1) : 0;  // A buffer; its previous use was j - kAB
+      bool ok = mbar_wait(wfull_bar(s), sphase, abort_flag);
+      if (ok && j >= kAB) ok = mbar_wait(aempty_bar(wg, ab), ((j / kAB) - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
       const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + s * T::kStageBytes);
-      const uint32_t a_addr = tmem + lane_off + 256 + wg * 64;
+      const uint32_t a_addr = tmem + lane_off + T::kACol0 + (wg * kAB + ab) * 64;
       if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
         for (int kt = 0; kt < kTcHalfKt; ++kt) {
@@ -226,67 +314,77 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(afull_bar(wg));
-        mbar_arrive(empty_bar(s));
+        mbar_arrive(wempty_bar(s));  // the weights of this stage have been read
+        mbar_arrive(afull_bar(wg, ab));
+      }
+      s += kWG;
+      if (s >= S) {
+        s -= S;
+        sphase ^= 1u;
       }
     }
-  } else if (warp == kTcMma) {
+  } else if (warp == T::kMma) {
     // ----------------------------------------------------------------- MMA
     // The whole warp runs the loop and one elected lane issues, so that the
-    // operands stay in uniform registers: issued from a lone lane, each MMA
-    // costs more than its tensor-core time at these sizes.
+    // operands stay in uniform registers.
     const uint32_t idesc = idesc_f16_f32(128, nslots);
-    // B descriptors: the first stage's xr slice, advanced in 16-byte units.
+    // B descriptors: box 0 (k-tiles 0-3) and box 1 (4-7) of the first
+    // stage's xr slice, advanced in 16-byte units.
     const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + T::kWBytes), 1024);
-    const uint32_t box_step = xr_box_bytes >> 4;
+    const uint64_t bdesc1 = bdesc0 + (xr_box_bytes >> 4);
     const uint32_t stage_step = static_cast<uint32_t>(T::kStageBytes) >> 4;
+    RingPos<S> rp;
+    int wg = 0, jw = 0;  // the warpgroup of half-unit q, and q / kWG
     bool stop = false;
     for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
       const long long bb = order.block(sg);
-      const int seg_lo = order.lo(bb);
-      const int seg_hi = order.hi(bb);
-      const int base = order.pos(sg, seg_lo) - seg_lo;  // processing position of unit i: base + i
-      // The accumulators must have been read out for the previous segment.
-      if (sg >= 1) {
+      const int n_seg_half = (order.hi(bb) - order.lo(bb)) * H;
+      const int base = order.pos(sg, order.lo(bb));  // processing position of the segment's first unit
+      const int dset = kAccB == 2 ? (sg & 1) : 0;
+      // The accumulator set must have been read out for its previous segment.
+      if (sg >= kAccB) {
         tc_fence_before();
-        if (!__all_sync(0xffffffffu, mbar_wait(dempty, (sg - 1) & 1, abort_flag))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(dempty_bar(dset), ((sg / kAccB) - 1) & 1, abort_flag))) break;
         tc_fence_after();
       }
-      uint32_t started = 0;  // bit g: chain g has had its first step
-      for (int i = seg_lo; i < seg_hi && !stop; ++i) {
-        const int k = base + i;
-        const int g = k & 1;  // the chain: units at even / odd processing positions
-        const uint32_t d_addr = tmem + g * 128;
-        for (int h = 0; h < H; ++h) {
-          const int q = k * H + h;
-          const int s = q % S;
-          const int wg = q % kTcWG, j = q / kTcWG;
-          bool ok = mbar_wait(full_bar(s), (q / S) & 1, abort_flag);
-          ok = ok && mbar_wait(afull_bar(wg), j & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = tmem + 256 + wg * 64;
-          const uint64_t bd = bdesc0 + s * stage_step;
-          const uint32_t acc0 = (started >> g) & 1u;
-          if (elect_one()) {
-#pragma unroll
-            for (int kt = 0; kt < kTcHalfKt; ++kt) {
-              // B: k-tile kt is inputs 16 (kt % 4) .. + 15 of the swizzled
-              // tile kt / 4 (rows of 128 bytes, 8-row groups 1024 apart).
-              mma_f16_tmemA(d_addr, a_addr + kt * 8, bd + (kt >> 2) * box_step + (kt & 3) * 2, idesc,
-                            kt > 0 ? 1u : acc0);
-            }
-            mma_commit(aempty_bar(wg));
-            mma_commit(empty_bar(s));
-          }
-          __syncwarp();
-          started |= 1u << g;
+      const uint32_t d_base = tmem + dset * 2 * SLOTS;
+      for (int i = 0; i < n_seg_half; ++i) {
+        const int g = ((base + i / H) & 1);  // chain: the unit's processing position parity
+        const int ab = kAB == 2 ? (jw & 1) : 0;
+        bool ok = mbar_wait(xfull_bar(rp.s), rp.phase, abort_flag);
+        ok = ok && mbar_wait(afull_bar(wg, ab), (jw / kAB) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_addr = d_base + g * SLOTS;
+        const uint32_t a_addr = tmem + T::kACol0 + (wg * kAB + ab) * 64;
+        const uint64_t bd0 = bdesc0 + rp.s * stage_step;
+        const uint64_t bd1 = bdesc1 + rp.s * stage_step;
+        // The chain's first step in the segment overwrites the accumulator:
+        // its first half-unit is the segment's first or second unit's half 0.
+        const bool first = (i / H) < 2 && (i % H) == 0;
+        if (elect_one()) {
+          mma_f16_tmemA(d_addr, a_addr, bd0, idesc, first ? 0u : 1u);
+          mma_f16_tmemA(d_addr, a_addr + 8, bd0 + 2, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 16, bd0 + 4, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 24, bd0 + 6, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 32, bd1, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
+          mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
+          mma_commit(aempty_bar(wg, ab));
+          mma_commit(xempty_bar(rp.s));
+        }
+        __syncwarp();
+        rp.next();
+        if (++wg == kWG) {
+          wg = 0;
+          ++jw;
         }
       }
-      if (elect_one()) mma_commit(dfull);
+      if (elect_one()) mma_commit(dfull_bar(dset));
       __syncwarp();
     }
     // Every MMA issued must have completed before Tensor Memory is freed.
@@ -294,8 +392,9 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     __syncwarp();
     volatile int never = 0;
     mbar_wait(drain, 0, &never);
-  } else {
+  } else if (warp < 4) {
     // ----------------------------------------------------------- epilogue
+    pdl_wait_prerequisites();  // partial sums, counters and y follow the kernel before
     const int t = threadIdx.x;  // output within the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     LinearPass lp;
@@ -315,7 +414,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
       // decode-row kernel.
       const bool has0 = (seg_hi - seg_lo >= 2) || ((base + seg_lo) % 2 == 0);
       const bool has1 = (seg_hi - seg_lo >= 2) || ((base + seg_lo) % 2 != 0);
-      const bool ok = mbar_wait_sleepy(dfull, sg & 1, abort_flag, 200);
+      const int dset = kAccB == 2 ? (sg & 1) : 0;
+      const bool ok = mbar_wait_sleepy(dfull_bar(dset), (sg / kAccB) & 1, abort_flag, 64);
       if (!group_all(1, 128, ok)) break;  // the named barriers below need all 128 threads
       tc_fence_after();
       const int c_first = cta_of_unit(static_cast<long long>(b) * order.UB, p.units, p.ctas);
@@ -327,14 +427,14 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
 #pragma unroll 1
       for (int r0 = 0; r0 < p.rows; r0 += 16) {
         float g0[16], g1[16];
-        tmem_ld16(tmem + lane_off + r0, g0);
-        tmem_ld16(tmem + lane_off + 128 + r0, g1);
+        tmem_ld16(tmem + lane_off + (dset * 2) * SLOTS + r0, g0);
+        tmem_ld16(tmem + lane_off + (dset * 2 + 1) * SLOTS + r0, g1);
 #pragma unroll
         for (int r = 0; r < 16; ++r) mine[(r0 + r) * 128 + t] = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dempty);  // the MMA thread may start the next segment
+      if (lane == 0) mbar_arrive(dempty_bar(dset));  // the MMA warp may reuse the set
       bool finish = true;
       if (shared) {
         __threadfence();
@@ -376,7 +476,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kTcMma) {
+  if (warp == T::kMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTcTmemCols);
   }
@@ -385,13 +485,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
 
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
 cudaError_t tc_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t err = cudaSuccess;
-  std::call_once(once, [] {
-    err = cudaFuncSetAttribute(trellis_linear_tc_kernel<BITS, LAYOUT, UKT, SLOTS>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BITS, SLOTS>::kBytes);
-  });
-  return err;
+  static PerDeviceOnce<kMaxAttrDevices> once;
+  return smem_attr_once(once, trellis_linear_tc_kernel<BITS, LAYOUT, UKT, SLOTS>, TcCfg<BITS, SLOTS>::kBytes);
 }
 
 // Launches the kernel of row-slot class SLOTS.
@@ -461,6 +556,7 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
   const int ns = tc_row_slots(lp.rows);
+  if (ns <= 16) return launch_tc<BITS, UKT, 16>(wmap, xmap, p, strips, ws.ctas, stream);
   if (ns <= 32) return launch_tc<BITS, UKT, 32>(wmap, xmap, p, strips, ws.ctas, stream);
   if (ns <= 64) return launch_tc<BITS, UKT, 64>(wmap, xmap, p, strips, ws.ctas, stream);
   return launch_tc<BITS, UKT, 128>(wmap, xmap, p, strips, ws.ctas, stream);

@@ -178,19 +178,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor, no swizzle, K-major: 8-row x 16-byte core
-// matrices; `lbo` = byte distance between core matrices adjacent in K, `sbo`
-// = between core matrices adjacent in M/N. Bits 46-47 hold the descriptor
-// version (1).
-__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
-  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
-}
-
 // Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of
 // 64 16-bit elements (128 bytes) at a 128-byte pitch, their 16-byte chunks
 // permuted by XOR with row % 8 (the order a tensor copy with the 128-byte
