@@ -95,28 +95,32 @@ def wait(bar, parity):
 # --------------------------------------------------------------------------
 # The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
 
-def run_tc(order, S, WG, H, rng, AB=1, ACC=1, plant=None):
+def run_tc(order, S, H, rng, ACC=2, plant=None):
     """The tcgen05 kernel: a weights producer and an xr producer, each
     refilling its part of a stage once that part's reader is done (the decode
-    warpgroup for the weights, the MMAs for xr); WG decode warpgroups with AB
-    A buffers each; one MMA warp; ACC accumulator sets alternating between
-    segments. `plant` names a fault to plant: "w_early" refills a stage's
-    weights without waiting for the decode, "x_early" refills its xr slice
-    without waiting for the MMAs."""
+    warpgroup for the weights, the MMAs for xr); four decode warpgroups
+    (half-unit q to warpgroup q mod 4) with one A buffer each; one MMA warp per
+    chain (units at even / odd processing positions), each issuing its
+    chain's MMAs in order; ACC accumulator sets alternating between segments.
+    `plant` names a fault to plant: "w_early" refills a stage's weights
+    without waiting for the decode, "x_early" its xr slice without waiting
+    for the MMAs, "no_dempty" starts a segment without waiting for the
+    readout of its accumulator set."""
+    WG = 4
     sim = Sim(rng)
     n_half = order.n_units * H
     wfull = [Bar("wfull%d" % s, 1) for s in range(S)]
     wempty = [Bar("wempty%d" % s, 4) for s in range(S)]
     xfull = [Bar("xfull%d" % s, 1) for s in range(S)]
     xempty = [Bar("xempty%d" % s, 1) for s in range(S)]
-    afull = [[Bar("afull%d.%d" % (w, b), 4) for b in range(AB)] for w in range(WG)]
-    aempty = [[Bar("aempty%d.%d" % (w, b), 1) for b in range(AB)] for w in range(WG)]
-    dfull = [Bar("dfull%d" % d, 1) for d in range(ACC)]
+    afull = [Bar("afull%d" % w, 4) for w in range(WG)]
+    aempty = [Bar("aempty%d" % w, 1) for w in range(WG)]
+    dfull = [Bar("dfull%d" % d, 2) for d in range(ACC)]
     dempty = [Bar("dempty%d" % d, 4) for d in range(ACC)]
     wtag = [None] * S        # half-unit whose weights a stage holds
     xtag = [None] * S        # half-unit whose xr slice a stage holds
-    abuf = [[None] * AB for _ in range(WG)]  # half-unit whose decoded weights an A buffer holds
-    acc = [None] * ACC       # segment whose sums an accumulator set holds
+    abuf = [None] * WG       # half-unit whose decoded weights an A buffer holds
+    acc = [[None, None] for _ in range(ACC)]  # segment whose sums a chain's accumulator holds
 
     def producer(full, empty, tag, wait_empty):
         for q in range(n_half):
@@ -135,52 +139,65 @@ def run_tc(order, S, WG, H, rng, AB=1, ACC=1, plant=None):
         while WG * j + wg < n_half:
             q = WG * j + wg
             s = q % S
-            ab = j % AB
             yield wait(wfull[s], (q // S) & 1)
-            if j >= AB:
-                yield wait(aempty[wg][ab], ((j // AB) - 1) & 1)
+            if j >= 1:
+                yield wait(aempty[wg], (j - 1) & 1)
             assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
-            abuf[wg][ab] = q
+            abuf[wg] = q
             yield None                                    # the decode takes a while
             assert wtag[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
             for _ in range(4):
                 wempty[s].arrive()
-                afull[wg][ab].arrive()
+                afull[wg].arrive()
             j += 1
 
-    def mma():
+    def segments():
         for sg in range(order.n_seg):
             bb = order.block(sg)
-            seg_lo, seg_hi = order.lo(bb), order.hi(bb)
-            base = order.pos(sg, seg_lo) - seg_lo
-            d = sg % ACC
-            if sg >= ACC:
-                yield wait(dempty[d], ((sg // ACC) - 1) & 1)
-            for i in range(seg_lo, seg_hi):
-                for h in range(H):
-                    q = (base + i) * H + h
-                    s, wg, j = q % S, q % WG, q // WG
-                    ab = j % AB
-                    yield wait(xfull[s], (q // S) & 1)
-                    yield wait(afull[wg][ab], (j // AB) & 1)
+            lo = order.lo(bb)
+            yield sg, order.pos(sg, lo), order.hi(bb) - lo
 
-                    def execute(q=q, s=s, wg=wg, ab=ab, sg=sg, d=d):
+    def mma(ch):
+        for sg, P, L in segments():
+            d = sg % ACC
+            if sg >= ACC and plant != "no_dempty":
+                yield wait(dempty[d], ((sg // ACC) - 1) & 1)
+            kf = P + ((ch - P) & 1)
+            if kf >= P + L:
+                dfull[d].arrive()                            # no unit of this chain here
+                continue
+            for k in range(kf, P + L, 2):
+                for h in range(H):
+                    q = k * H + h
+                    s, wg = q % S, q % WG
+                    assert ((q // H) & 1) == ch
+                    yield wait(xfull[s], (q // S) & 1)
+                    yield wait(afull[wg], (q // WG) & 1)
+
+                    def execute(q=q, s=s, wg=wg, sg=sg, d=d, first=(k == kf and h == 0)):
                         assert xtag[s] == q, "MMA of %d found stage %d's xr of %s" % (q, s, xtag[s])
-                        assert abuf[wg][ab] == q, "MMA of %d found A buffer %d.%d holding %s" % (
-                            q, wg, ab, abuf[wg][ab])
-                        acc[d] = sg
-                        aempty[wg][ab].arrive()              # the two commits after the MMAs
+                        assert abuf[wg] == q, "MMA of %d found A buffer %d holding %s" % (q, wg, abuf[wg])
+                        if first:
+                            acc[d][ch] = sg
+                        assert acc[d][ch] == sg, "chain %d MMA of segment %d into sums of %s" % (
+                            ch, sg, acc[d][ch])
+                        aempty[wg].arrive()                  # the two commits after the MMAs
                         xempty[s].arrive()
                     sim.tensor.append(execute)
             sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
 
     def epilogue():
-        for sg in range(order.n_seg):
+        for sg, P, L in segments():
             d = sg % ACC
             yield wait(dfull[d], (sg // ACC) & 1)
-            assert acc[d] == sg, "segment %d read accumulators of %s" % (sg, acc[d])
+            has = [L >= 2 or P % 2 == ch for ch in range(2)]
+            for ch in range(2):
+                if has[ch]:
+                    assert acc[d][ch] == sg, "segment %d read chain %d sums of %s" % (sg, ch, acc[d][ch])
             yield None                                    # the readout takes a while
-            assert acc[d] == sg, "accumulators of segment %d overwritten during readout" % sg
+            for ch in range(2):
+                if has[ch]:
+                    assert acc[d][ch] == sg, "chain %d sums of segment %d overwritten" % (ch, sg)
             for _ in range(4):
                 dempty[d].arrive()
 
@@ -188,7 +205,8 @@ def run_tc(order, S, WG, H, rng, AB=1, ACC=1, plant=None):
     sim.add(producer(xfull, xempty, xtag, plant != "x_early"))
     for wg in range(WG):
         sim.add(decode(wg))
-    sim.add(mma())
+    sim.add(mma(0))
+    sim.add(mma(1))
     sim.add(epilogue())
     sim.run()
     assert all(wtag[s] is not None for s in range(min(S, n_half)))
@@ -272,25 +290,25 @@ def cta_orders(seed, n):
         yield SegmentOrder(u0, u1, ub)
 
 
-@pytest.mark.parametrize("S,WG,H,AB,ACC", [(18, 3, 2, 2, 2), (12, 3, 2, 2, 2), (9, 3, 2, 2, 1), (6, 3, 1, 2, 2),
-                                            (4, 4, 2, 1, 1), (8, 4, 1, 1, 1), (12, 3, 2, 1, 1)])
-def test_tc_kernel_protocol_under_random_schedules(S, WG, H, AB, ACC):
-    rng = random.Random(100 * S + 10 * WG + H + 1000 * AB + 10000 * ACC)
-    for order in cta_orders(S * WG + H, 60):
+@pytest.mark.parametrize("S,H,ACC", [(16, 2, 2), (12, 2, 2), (8, 2, 2), (4, 2, 1), (8, 1, 2), (4, 1, 1), (12, 1, 2)])
+def test_tc_kernel_protocol_under_random_schedules(S, H, ACC):
+    rng = random.Random(100 * S + 10 * H + ACC)
+    for order in cta_orders(S * 4 + H, 60):
         for _ in range(3):
-            run_tc(order, S, WG, H, rng, AB, ACC)
+            run_tc(order, S, H, rng, ACC)
 
 
-@pytest.mark.parametrize("plant", ["w_early", "x_early"])
-def test_tc_planted_early_refills_are_caught(plant):
+@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty"])
+def test_tc_planted_faults_are_caught(plant):
     """A producer that refills its part of a stage without waiting for that
-    part's reader must fail some schedule."""
+    part's reader, or a chain that starts a segment in an accumulator set
+    the epilogue may still be reading, must fail some schedule."""
     rng = random.Random(21)
     failures = 0
-    for order in cta_orders(21, 40):
+    for order in cta_orders(21, 60):
         for _ in range(5):
             try:
-                run_tc(order, 6, 3, 2, rng, 2, 2, plant=plant)
+                run_tc(order, 8, 2, rng, 1 if plant == "no_dempty" else 2, plant=plant)
             except AssertionError:
                 failures += 1
     assert failures > 0
@@ -305,17 +323,16 @@ def test_mma_kernel_protocol_under_random_schedules(S):
 
 
 def test_planted_fault_is_caught():
-    """Stages that are not a multiple of the consumers: a stage's previous
-    half-unit went to another warpgroup, so a warpgroup can wait for a
-    stage's next copy before its previous one has landed, and the parity
-    wait passes on the wrong phase. Some schedule must fail (about one in
-    two hundred does, so many are run)."""
+    """A stage count that is not a multiple of the four decode warpgroups: a
+    stage's previous half-unit went to another warpgroup (and possibly the
+    other chain), so a wait can pass on the wrong phase. Some schedule must
+    fail."""
     rng = random.Random(7)
     failures = 0
     for order in cta_orders(7, 400):
         for _ in range(5):
             try:
-                run_tc(order, 5, 4, 2, rng)
+                run_tc(order, 6, 2, rng, 2)
             except AssertionError:
                 failures += 1
     assert failures > 0

@@ -103,10 +103,10 @@ def mma_stages(bits, ukt, budget=196 * KIB):
 
 def tc_stages(bits, slots, budget=227 * KIB):
     """Stage count and decode warpgroups of the tcgen05 kernel's class."""
-    wg = 3 if slots <= 64 else 4
+    wg = 4
     stage = 256 * bits * 8 + slots * 16 * 8 * 2
     fit = (budget - 8192 - 2048) // stage
-    return (min(fit, 18) // wg) * wg, wg
+    return (min(fit, 16) // wg) * wg, wg
 
 
 def ranges(units, ctas):
@@ -167,15 +167,18 @@ def test_stage_counts_keep_each_stage_with_one_consumer(bits):
         s, wg = tc_stages(bits, slots)
         assert s >= wg and s % wg == 0, (bits, slots, s)
         # Half-unit q is decoded by warpgroup q % wg from stage q % s, so the
-        # stage's previous half-unit q - s went to the same warpgroup.
+        # stage's previous half-unit q - s went to the same warpgroup, and
+        # (two half-units a unit, units alternating between the chains) to
+        # the same chain.
         for q in range(s, 4 * s):
             assert (q - s) % wg == q % wg
+            assert ((q - s) // 2) % 2 == (q // 2) % 2 and (q - s) % 2 == q % 2
 
 
 def test_stage_counts_of_the_measured_classes():
     """The counts the measurements were taken with (4 bits)."""
     assert mma_stages(4, 16) == 6
-    assert tc_stages(4, 16) == (18, 3)
-    assert tc_stages(4, 32) == (12, 3)
-    assert tc_stages(4, 64) == (9, 3)
+    assert tc_stages(4, 16) == (16, 4)
+    assert tc_stages(4, 32) == (12, 4)
+    assert tc_stages(4, 64) == (8, 4)
     assert tc_stages(4, 128) == (4, 4)

@@ -27,19 +27,25 @@
 //               Memory, added, written to this CTA's partial-sum slot, then
 //               (when the CTA owns the block, or arrives last) the output
 //               rotation, svh and the stores
-//   warps 4-    decode: three warpgroups (four at 128 row slots) take
-//               half-units (8 k-tiles) in turn; thread n decodes output n's
+//   warps 4-19  decode: four warpgroups take half-units (8 k-tiles) in turn,
+//               half-unit q going to warpgroup q mod 4, so that a warpgroup
+//               only decodes units of one chain; thread n decodes output n's
 //               16 weights of each k-tile into Tensor Memory lane n (the MMA's
-//               A operand), in one of its warpgroup's A buffers
+//               A operand), in its warpgroup's A buffer
 //   next warp   weights producer: one thread copies each half-unit's packed
 //               weights into the stage ring as soon as the decode of the
 //               stage's previous half-unit is done
 //   next warp   xr producer: one thread copies each half-unit's xr slice
-//               (two tensor copies of 64 inputs x the pass's row slots, with
-//               the 128-byte swizzle: the MMA's K-major B layout) as soon as
-//               the MMAs of the stage's previous half-unit are done
-//   last warp   MMA: allocates Tensor Memory; the warp runs the MMA loop and
-//               one elected lane issues
+//               (one tensor copy of two chunks of 64 inputs x the pass's row
+//               slots, with the 128-byte swizzle: the MMA's K-major B layout)
+//               as soon as the MMAs of the stage's previous half-unit are done
+//   last two    MMA, one warp per chain: each issues its chain's MMAs in
+//               input order (one elected lane of the whole warp); the first
+//               allocates Tensor Memory. At 16 row slots an MMA costs the
+//               tensor pipe about 40 cycles whatever N, so the MMAs of a
+//               half-unit take about as long as the decode warps need to
+//               decode the next one; one issuing warp for both chains was
+//               busy most of the time and held the decode up.
 // A stage holds a half-unit's weights and its xr slice, each part with its
 // own full and empty barriers: the weights are read by the decode and the
 // xr slice by the MMAs, so each part is refilled as soon as its reader is
@@ -70,39 +76,41 @@ constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared bloc
 
 // Shared memory and Tensor Memory of a pass class (SLOTS = 16, 32, 64 or 128
 // row slots): a stage holds a half-unit's packed weights and its xr slice for
-// SLOTS row slots, so fewer slots make smaller stages and more of them (18 /
-// 12 / 9 / 4 at 4 bits).
+// SLOTS row slots, so fewer slots make smaller stages and more of them (16 /
+// 12 / 8 / 4 at 4 bits).
 template <int BITS, int SLOTS>
 struct TcCfg {
   static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
   static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // SLOTS rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
-  // Decode warpgroups: three up to 64 row slots, four at 128 (measured at 4
-  // and 6 bits).
-  static constexpr int kWG = SLOTS <= 64 ? 3 : 4;
+  // Four decode warpgroups: half-unit q goes to warpgroup q mod 4, so a
+  // warpgroup only ever decodes units of one chain (units at even or at odd
+  // processing positions), and the chain's MMA warp is the only reader of
+  // its A buffer.
+  static constexpr int kWG = 4;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
-  // to the same decode warpgroup.
-  static constexpr int kStages = (kStagesFit < 18 ? kStagesFit : 18) / kWG * kWG;
+  // to the same decode warpgroup (and the same chain).
+  static constexpr int kStages = (kStagesFit < 16 ? kStagesFit : 16) / kWG * kWG;
+  static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
   // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
   // in kAccBufs sets that alternate between segments (so that the MMAs of a
-  // segment can start while the epilogue reads the previous one), then
-  // kABufs A buffers of 64 columns (8 k-tiles) per decode warpgroup (so that
-  // a warpgroup decodes its next half-unit while the MMAs read its last).
-  static constexpr int kAccBufs = SLOTS <= 32 ? 2 : 1;
-  static constexpr int kABufs = SLOTS <= 64 ? 2 : 1;
+  // segment can start while the epilogue reads the previous one), then one
+  // A buffer of 64 columns (8 k-tiles) per decode warpgroup.
+  static constexpr int kAccBufs = SLOTS <= 64 ? 2 : 1;
   static constexpr int kACol0 = kAccBufs * 2 * SLOTS;
-  static_assert(kACol0 + kWG * kABufs * 64 <= kTcTmemCols, "Tensor Memory columns");
-  // Warp roles: epilogue 0-3, decode, weights producer, xr producer, MMA.
+  static_assert(kACol0 + kWG * 64 <= kTcTmemCols, "Tensor Memory columns");
+  // Warp roles: epilogue 0-3, decode 4-19, weights producer, xr producer,
+  // and one MMA warp per chain.
   static constexpr int kProdW = 4 + 4 * kWG;
   static constexpr int kProdX = kProdW + 1;
-  static constexpr int kMma = kProdX + 1;
-  static constexpr int kThreads = (kMma + 1) * 32;
+  static constexpr int kMma = kProdX + 1;  // chain 0; chain 1 is the next warp
+  static constexpr int kThreads = (kMma + 2) * 32;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
-  // wfull, wempty, xfull, xempty per stage; afull, aempty per A buffer;
-  // dfull, dempty per accumulator set; drain
-  static constexpr int kNumBars = 4 * kStages + 2 * kWG * kABufs + 2 * kAccBufs + 1;
+  // wfull, wempty, xfull, xempty per stage; afull, aempty per decode
+  // warpgroup; dfull, dempty per accumulator set; drain
+  static constexpr int kNumBars = 4 * kStages + 2 * kWG + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
   static_assert(kBytes <= kSmemBudgetWide, "shared memory");
@@ -144,7 +152,6 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
   constexpr int S = T::kStages;
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
   constexpr int kWG = T::kWG;
-  constexpr int kAB = T::kABufs;
   constexpr int kAccB = T::kAccBufs;
   static_assert(S >= kWG && S % kWG == 0, "stages must stay with one decode warpgroup");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -158,10 +165,10 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
   auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
   auto xempty_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
   const uint32_t abar0 = bar0 + 8u * (4 * S);
-  // A buffer b of warpgroup w; accumulator set d.
-  auto afull_bar = [&](int w, int b) { return abar0 + 8u * (w * kAB + b); };
-  auto aempty_bar = [&](int w, int b) { return abar0 + 8u * (kWG * kAB + w * kAB + b); };
-  const uint32_t dbar0 = abar0 + 8u * (2 * kWG * kAB);
+  // The A buffer of warpgroup w; accumulator set d.
+  auto afull_bar = [&](int w) { return abar0 + 8u * w; };
+  auto aempty_bar = [&](int w) { return abar0 + 8u * (kWG + w); };
+  const uint32_t dbar0 = abar0 + 8u * (2 * kWG);
   auto dfull_bar = [&](int d) { return dbar0 + 8u * d; };
   auto dempty_bar = [&](int d) { return dbar0 + 8u * (kAccB + d); };
   const uint32_t drain = dbar0 + 8u * (2 * kAccB);
@@ -186,16 +193,15 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
       mbar_init(xfull_bar(s), 1);
       mbar_init(xempty_bar(s), 1);  // the MMAs' commit
     }
-    for (int w = 0; w < kWG; ++w)
-      for (int b = 0; b < kAB; ++b) {
-        mbar_init(afull_bar(w, b), 4);
-        mbar_init(aempty_bar(w, b), 1);
-      }
+    for (int w = 0; w < kWG; ++w) {
+      mbar_init(afull_bar(w), 4);
+      mbar_init(aempty_bar(w), 1);
+    }
     for (int d = 0; d < kAccB; ++d) {
-      mbar_init(dfull_bar(d), 1);
+      mbar_init(dfull_bar(d), 2);  // one signal per chain
       mbar_init(dempty_bar(d), 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     fence_barrier_init();
   }
   if (warp == T::kMma) {
@@ -257,8 +263,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
         const uint32_t st = smem_u32(smem + rp.s * T::kStageBytes) + T::kWBytes;
         const int xi = x0 + h * kTcHalfKt * 16;
         mbar_arrive_expect_tx(xfull_bar(rp.s), 2 * xr_box_bytes);
-        tma_load_2d(st, &xmap, xi, 0, xfull_bar(rp.s));
-        tma_load_2d(st + xr_box_bytes, &xmap, xi + 64, 0, xfull_bar(rp.s));
+        tma_load_3d(st, &xmap, 0, 0, xi >> 6, xfull_bar(rp.s));  // both 64-input chunks at once
         issued = q + 1;
         rp.next();
         if (++h == H) {
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     }
   } else if (warp >= 4 && warp < T::kProdW) {
     // -------------------------------------------------------------- decode
-    const int wg = (warp - 4) >> 2;              // takes half-units wg, wg + kWG, ...
+    const int wg = (warp - 4) >> 2;              // takes half-units wg, wg + 4, ...
     const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
     const int tile = n >> 4, col = n & 15;
@@ -283,12 +288,12 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     for (int j = 0;; ++j) {
       const int q = kWG * j + wg;
       if (q >= n_half) break;
-      const int ab = kAB == 2 ? (j & 1) : 0;  // A buffer; its previous use was j - kAB
       bool ok = mbar_wait(wfull_bar(s), sphase, abort_flag);
-      if (ok && j >= kAB) ok = mbar_wait(aempty_bar(wg, ab), ((j / kAB) - 1) & 1, abort_flag);
+      // The A buffer: its previous half-unit's MMAs must be done.
+      if (ok && j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
       const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + s * T::kStageBytes);
-      const uint32_t a_addr = tmem + lane_off + T::kACol0 + (wg * kAB + ab) * 64;
+      const uint32_t a_addr = tmem + lane_off + T::kACol0 + wg * 64;
       if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
         for (int kt = 0; kt < kTcHalfKt; ++kt) {
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(wempty_bar(s));  // the weights of this stage have been read
-        mbar_arrive(afull_bar(wg, ab));
+        mbar_arrive(afull_bar(wg));
       }
       s += kWG;
       if (s >= S) {
@@ -323,75 +328,80 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
         sphase ^= 1u;
       }
     }
-  } else if (warp == T::kMma) {
-    // ----------------------------------------------------------------- MMA
+  } else if (warp == T::kMma || warp == T::kMma + 1) {
+    // -------------------------------------------------- MMA, one per chain
     // The whole warp runs the loop and one elected lane issues, so that the
-    // operands stay in uniform registers.
+    // operands stay in uniform registers. Each chain's MMAs are issued in
+    // input order by its own warp; the two chains' accumulators are
+    // independent, so the two warps need no order between them.
+    const int ch = warp - T::kMma;  // units at processing positions ch, ch + 2, ...
     const uint32_t idesc = idesc_f16_f32(128, nslots);
     // B descriptors: box 0 (k-tiles 0-3) and box 1 (4-7) of the first
     // stage's xr slice, advanced in 16-byte units.
     const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + T::kWBytes), 1024);
     const uint64_t bdesc1 = bdesc0 + (xr_box_bytes >> 4);
     const uint32_t stage_step = static_cast<uint32_t>(T::kStageBytes) >> 4;
-    RingPos<S> rp;
-    int wg = 0, jw = 0;  // the warpgroup of half-unit q, and q / kWG
     bool stop = false;
     for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
       const long long bb = order.block(sg);
-      const int n_seg_half = (order.hi(bb) - order.lo(bb)) * H;
-      const int base = order.pos(sg, order.lo(bb));  // processing position of the segment's first unit
+      const int seg_lo = order.lo(bb);
+      const int P = order.pos(sg, seg_lo);  // the segment's processing positions: [P, P + L)
+      const int L = order.hi(bb) - seg_lo;
       const int dset = kAccB == 2 ? (sg & 1) : 0;
-      // The accumulator set must have been read out for its previous segment.
+      // The accumulator set must have been read out for its previous segment
+      // (waited for every segment in order, so no wait skips a phase).
       if (sg >= kAccB) {
         tc_fence_before();
         if (!__all_sync(0xffffffffu, mbar_wait(dempty_bar(dset), ((sg / kAccB) - 1) & 1, abort_flag))) break;
         tc_fence_after();
       }
-      const uint32_t d_base = tmem + dset * 2 * SLOTS;
-      for (int i = 0; i < n_seg_half; ++i) {
-        const int g = ((base + i / H) & 1);  // chain: the unit's processing position parity
-        const int ab = kAB == 2 ? (jw & 1) : 0;
-        bool ok = mbar_wait(xfull_bar(rp.s), rp.phase, abort_flag);
-        ok = ok && mbar_wait(afull_bar(wg, ab), (jw / kAB) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          stop = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_addr = d_base + g * SLOTS;
-        const uint32_t a_addr = tmem + T::kACol0 + (wg * kAB + ab) * 64;
-        const uint64_t bd0 = bdesc0 + rp.s * stage_step;
-        const uint64_t bd1 = bdesc1 + rp.s * stage_step;
-        // The chain's first step in the segment overwrites the accumulator:
-        // its first half-unit is the segment's first or second unit's half 0.
-        const bool first = (i / H) < 2 && (i % H) == 0;
-        if (elect_one()) {
-          mma_f16_tmemA(d_addr, a_addr, bd0, idesc, first ? 0u : 1u);
-          mma_f16_tmemA(d_addr, a_addr + 8, bd0 + 2, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 16, bd0 + 4, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 24, bd0 + 6, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 32, bd1, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
-          mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
-          mma_commit(aempty_bar(wg, ab));
-          mma_commit(xempty_bar(rp.s));
-        }
+      const int kf = P + ((ch - P) & 1);  // the chain's first position in the segment
+      if (kf >= P + L) {
+        // No unit of this chain here (its sum counts as +0): a plain arrival.
+        if (lane == 0) mbar_arrive(dfull_bar(dset));
         __syncwarp();
-        rp.next();
-        if (++wg == kWG) {
-          wg = 0;
-          ++jw;
+        continue;
+      }
+      const uint32_t d_addr = tmem + (dset * 2 + ch) * SLOTS;
+      for (int k = kf; k < P + L && !stop; k += 2) {
+#pragma unroll 1
+        for (int h = 0; h < H; ++h) {
+          const int q = k * H + h;
+          const int s = q % S;
+          const int wg = q & (kWG - 1);
+          bool ok = mbar_wait(xfull_bar(s), (q / S) & 1, abort_flag);
+          ok = ok && mbar_wait(afull_bar(wg), (q / kWG) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = tmem + T::kACol0 + wg * 64;
+          const uint64_t bd0 = bdesc0 + s * stage_step;
+          const uint64_t bd1 = bdesc1 + s * stage_step;
+          const bool first = k == kf && h == 0;  // overwrites the accumulator
+          if (elect_one()) {
+            mma_f16_tmemA(d_addr, a_addr, bd0, idesc, first ? 0u : 1u);
+            mma_f16_tmemA(d_addr, a_addr + 8, bd0 + 2, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 16, bd0 + 4, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 24, bd0 + 6, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 32, bd1, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
+            mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
+            mma_commit(aempty_bar(wg));
+            mma_commit(xempty_bar(s));
+          }
+          __syncwarp();
         }
       }
+      if (stop) break;
       if (elect_one()) mma_commit(dfull_bar(dset));
       __syncwarp();
     }
     // Every MMA issued must have completed before Tensor Memory is freed.
     if (elect_one()) mma_commit(drain);
     __syncwarp();
-    volatile int never = 0;
-    mbar_wait(drain, 0, &never);
   } else if (warp < 4) {
     // ----------------------------------------------------------- epilogue
     pdl_wait_prerequisites();  // partial sums, counters and y follow the kernel before
@@ -477,6 +487,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == T::kMma) {
+    volatile int never = 0;
+    mbar_wait(drain, 0, &never);  // both chains' MMAs have completed
     tc_fence_after();
     tmem_dealloc(tmem, kTcTmemCols);
   }
@@ -529,14 +541,15 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
       return cudaErrorInvalidValue;
   }
   {
-    // xr [rows][in] fp16; a box is 64 inputs (128 bytes) x the pass's row
-    // slots, written with the 128-byte swizzle: the MMA's K-major B operand
-    // for 4 k-tiles. Slots past `rows` are filled with zeros.
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.in_features), static_cast<cuuint64_t>(lp.rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.in_features) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(tc_row_slots(lp.rows))};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(lp.xr), dims, strides, box,
+    // xr [rows][in] fp16 viewed as (64 inputs, rows, in / 64): a box of
+    // (64, the pass's row slots, 2) lands as two chunks of 64 inputs (the
+    // MMA's K-major B operand for 4 k-tiles each), each the row slots' 128-byte
+    // rows written with the 128-byte swizzle; slots past `rows` are zeros.
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows), static_cast<cuuint64_t>(lp.in_features / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tc_row_slots(lp.rows)), 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
