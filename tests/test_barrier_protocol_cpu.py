@@ -97,8 +97,9 @@ def wait(bar, parity):
 
 def run_tc(order, S, H, rng, ACC=2, plant=None):
     """The tcgen05 kernel: a weights producer and an xr producer, each
-    refilling its part of a stage once that part's reader is done (the decode
-    warpgroup for the weights, the MMAs for xr); four decode warpgroups
+    refilling its part of a unit's stages (one copy per unit of H half-units)
+    once that part's readers are done (the decode warpgroups for the
+    weights, the MMAs for xr); four decode warpgroups
     (half-unit q to warpgroup q mod 4) with one A buffer each; one MMA warp per
     chain (units at even / odd processing positions), each issuing its
     chain's MMAs in order; ACC accumulator sets alternating between segments.
@@ -109,10 +110,12 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
     WG = 4
     sim = Sim(rng)
     n_half = order.n_units * H
-    wfull = [Bar("wfull%d" % s, 1) for s in range(S)]
-    wempty = [Bar("wempty%d" % s, 4) for s in range(S)]
-    xfull = [Bar("xfull%d" % s, 1) for s in range(S)]
-    xempty = [Bar("xempty%d" % s, 1) for s in range(S)]
+    CG = H if S >= 8 else 1  # half-units per copy: a unit where the ring is deep enough
+    SU = S // CG             # copy slots: the barriers go by copies
+    wfull = [Bar("wfull%d" % s, 1) for s in range(SU)]
+    wempty = [Bar("wempty%d" % s, 4 * CG) for s in range(SU)]
+    xfull = [Bar("xfull%d" % s, 1) for s in range(SU)]
+    xempty = [Bar("xempty%d" % s, CG) for s in range(SU)]
     afull = [Bar("afull%d" % w, 4) for w in range(WG)]
     aempty = [Bar("aempty%d" % w, 1) for w in range(WG)]
     dfull = [Bar("dfull%d" % d, 2) for d in range(ACC)]
@@ -123,15 +126,16 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
     acc = [[None, None] for _ in range(ACC)]  # segment whose sums a chain's accumulator holds
 
     def producer(full, empty, tag, wait_empty):
-        for q in range(n_half):
-            s = q % S
-            if q >= S and wait_empty:
-                yield wait(empty[s], ((q // S) - 1) & 1)
-            full[s].arrive_expect_tx(1)
+        for u in range(n_half // CG):
+            us = u % SU
+            if u >= SU and wait_empty:
+                yield wait(empty[us], ((u // SU) - 1) & 1)
+            full[us].arrive_expect_tx(1)
 
-            def land(s=s, q=q):
-                tag[s] = q
-                full[s].complete_tx(1)
+            def land(us=us, u=u):
+                for h in range(CG):
+                    tag[us * CG + h] = u * CG + h
+                full[us].complete_tx(1)
             sim.copies.append(land)
 
     def decode(wg):
@@ -139,7 +143,7 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
         while WG * j + wg < n_half:
             q = WG * j + wg
             s = q % S
-            yield wait(wfull[s], (q // S) & 1)
+            yield wait(wfull[s // CG], (q // S) & 1)
             if j >= 1:
                 yield wait(aempty[wg], (j - 1) & 1)
             assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
@@ -147,7 +151,7 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
             yield None                                    # the decode takes a while
             assert wtag[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
             for _ in range(4):
-                wempty[s].arrive()
+                wempty[s // CG].arrive()
                 afull[wg].arrive()
             j += 1
 
@@ -171,7 +175,7 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
                     q = k * H + h
                     s, wg = q % S, q % WG
                     assert ((q // H) & 1) == ch
-                    yield wait(xfull[s], (q // S) & 1)
+                    yield wait(xfull[s // CG], (q // S) & 1)
                     yield wait(afull[wg], (q // WG) & 1)
 
                     def execute(q=q, s=s, wg=wg, sg=sg, d=d, first=(k == kf and h == 0)):
@@ -182,7 +186,7 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
                         assert acc[d][ch] == sg, "chain %d MMA of segment %d into sums of %s" % (
                             ch, sg, acc[d][ch])
                         aempty[wg].arrive()                  # the two commits after the MMAs
-                        xempty[s].arrive()
+                        xempty[s // CG].arrive()
                     sim.tensor.append(execute)
             sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
 

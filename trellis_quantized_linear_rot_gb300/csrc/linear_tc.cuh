@@ -78,7 +78,7 @@ constexpr int kTcPartialSlots = 3;  // first block, last block, an unshared bloc
 // row slots): a stage holds a half-unit's packed weights and its xr slice for
 // SLOTS row slots, so fewer slots make smaller stages and more of them (16 /
 // 12 / 8 / 4 at 4 bits).
-template <int BITS, int SLOTS>
+template <int BITS, int SLOTS, int H>
 struct TcCfg {
   static constexpr int kWBytes = 256 * BITS * kTcHalfKt;       // 8 k-tiles x 8 tiles x 32*BITS bytes
   static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // SLOTS rows x 128 inputs, fp16
@@ -93,6 +93,14 @@ struct TcCfg {
   // to the same decode warpgroup (and the same chain).
   static constexpr int kStages = (kStagesFit < 16 ? kStagesFit : 16) / kWG * kWG;
   static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
+  // The stages hold half-units, but the copies and their barriers go by
+  // groups of CG half-units (contiguous in both rings): a whole unit where
+  // the ring is deep enough, so that each producer issues one copy a unit;
+  // single half-units at 128 row slots, whose ring holds only four.
+  static constexpr int CG = kStages >= 8 ? H : 1;
+  static constexpr int kUnitSlots = kStages / CG;
+  static constexpr int kWRingOff = 0;                          // [kStages][kWBytes]
+  static constexpr int kXRingOff = kStages * kWBytes;          // [kStages][kXrBytes], 1024-byte aligned
   // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
   // in kAccBufs sets that alternate between segments (so that the MMAs of a
   // segment can start while the epilogue reads the previous one), then one
@@ -108,9 +116,9 @@ struct TcCfg {
   static constexpr int kThreads = (kMma + 2) * 32;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
-  // wfull, wempty, xfull, xempty per stage; afull, aempty per decode
+  // wfull, wempty, xfull, xempty per unit slot; afull, aempty per decode
   // warpgroup; dfull, dempty per accumulator set; drain
-  static constexpr int kNumBars = 4 * kStages + 2 * kWG + 2 * kAccBufs + 1;
+  static constexpr int kNumBars = 4 * kUnitSlots + 2 * kWG + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
   static_assert(kBytes <= kSmemBudgetWide, "shared memory");
@@ -145,12 +153,14 @@ struct RingPos {
 };
 
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
-__global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads, 1)
     trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                              const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
-  using T = TcCfg<BITS, SLOTS>;
-  constexpr int S = T::kStages;
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
+  using T = TcCfg<BITS, SLOTS, H>;
+  constexpr int S = T::kStages;
+  constexpr int CG = T::CG;           // half-units per copy
+  constexpr int SU = T::kUnitSlots;   // copy slots
   constexpr int kWG = T::kWG;
   constexpr int kAccB = T::kAccBufs;
   static_assert(S >= kWG && S % kWG == 0, "stages must stay with one decode warpgroup");
@@ -160,11 +170,12 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + T::kMiscOff + 8);
-  auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
-  auto wempty_bar = [&](int s) { return bar0 + 8u * (S + s); };
-  auto xfull_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto xempty_bar = [&](int s) { return bar0 + 8u * (3 * S + s); };
-  const uint32_t abar0 = bar0 + 8u * (4 * S);
+  // Barriers of copy slot us (holding half-unit stages us * CG .. + CG - 1).
+  auto wfull_bar = [&](int us) { return bar0 + 8u * us; };
+  auto wempty_bar = [&](int us) { return bar0 + 8u * (SU + us); };
+  auto xfull_bar = [&](int us) { return bar0 + 8u * (2 * SU + us); };
+  auto xempty_bar = [&](int us) { return bar0 + 8u * (3 * SU + us); };
+  const uint32_t abar0 = bar0 + 8u * (4 * SU);
   // The A buffer of warpgroup w; accumulator set d.
   auto afull_bar = [&](int w) { return abar0 + 8u * w; };
   auto aempty_bar = [&](int w) { return abar0 + 8u * (kWG + w); };
@@ -187,11 +198,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     // are multiples of 1024).
     *abort_flag = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
     *last_flag = 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(wfull_bar(s), 1);
-      mbar_init(wempty_bar(s), 4);  // the decoding warpgroup's 4 warps
-      mbar_init(xfull_bar(s), 1);
-      mbar_init(xempty_bar(s), 1);  // the MMAs' commit
+    for (int us = 0; us < SU; ++us) {
+      mbar_init(wfull_bar(us), 1);
+      mbar_init(wempty_bar(us), 4 * CG);  // the 4 warps of each half-unit's decoding warpgroup
+      mbar_init(xfull_bar(us), 1);
+      mbar_init(xempty_bar(us), CG);      // the MMAs' commit, per half-unit
     }
     for (int w = 0; w < kWG; ++w) {
       mbar_init(afull_bar(w), 4);
@@ -217,64 +228,65 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
 
   if (warp == T::kProdW) {
     // ---------------------------------------------------- weights producer
-    // The weights are not written by the kernel before this one, so their
-    // copies start at once.
+    // One copy per group of CG half-units (contiguous stages). The weights
+    // are not written by the kernel before this one, so their copies start
+    // at once.
     if (lane == 0) {
       UnitCursor cur(order);
-      RingPos<S> rp;
-      int h = 0;
-      const uint8_t* unit_src = p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT);
-      int kt0 = cur.ub() * UKT;
+      RingPos<SU> rp;
+      int h0 = 0;  // first half-unit of the group within its unit
       int issued = 0;
-      for (int q = 0; q < n_half; ++q) {
-        if (q >= S && !mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
-        const uint32_t st = smem_u32(smem + rp.s * T::kStageBytes);
-        mbar_arrive_expect_tx(wfull_bar(rp.s), T::kWBytes);
+      const int n_groups = n_half / CG;
+      for (int u = 0; u < n_groups; ++u) {
+        if (u >= SU && !mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
+        const uint32_t st = smem_u32(smem + T::kWRingOff + rp.s * CG * T::kWBytes);
+        mbar_arrive_expect_tx(wfull_bar(rp.s), CG * T::kWBytes);
         if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, kt0 + h * kTcHalfKt, wfull_bar(rp.s));
+          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT + h0 * kTcHalfKt,
+                      wfull_bar(rp.s));
         else
-          bulk_load_1d(st, unit_src + h * T::kWBytes, T::kWBytes, wfull_bar(rp.s));
-        issued = q + 1;
+          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h0 * T::kWBytes,
+                       CG * T::kWBytes, wfull_bar(rp.s));
+        issued = u + 1;
         rp.next();
-        if (++h == H) {
-          h = 0;
+        h0 += CG;
+        if (h0 == H) {
+          h0 = 0;
           cur.next();
-          unit_src = p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT);
-          kt0 = cur.ub() * UKT;
         }
       }
       // Let every copy this thread started land before the CTA can exit.
-      for (int q = issued - S > 0 ? issued - S : 0; q < issued; ++q) {
+      for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
         volatile int never = 0;
-        mbar_wait(wfull_bar(q % S), (q / S) & 1, &never);
+        mbar_wait(wfull_bar(u % SU), (u / SU) & 1, &never);
       }
     }
   } else if (warp == T::kProdX) {
     // --------------------------------------------------------- xr producer
+    // One copy per group of CG half-units: their 2 CG chunks of 64 inputs.
     if (lane == 0) {
       pdl_wait_prerequisites();  // xr is written by the kernel before this one
       UnitCursor cur(order);
-      RingPos<S> rp;
-      int h = 0;
-      int x0 = cur.ub() * UKT * 16;  // first input of the unit
+      RingPos<SU> rp;
+      int h0 = 0;
       int issued = 0;
-      for (int q = 0; q < n_half; ++q) {
-        if (q >= S && !mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
-        const uint32_t st = smem_u32(smem + rp.s * T::kStageBytes) + T::kWBytes;
-        const int xi = x0 + h * kTcHalfKt * 16;
-        mbar_arrive_expect_tx(xfull_bar(rp.s), 2 * xr_box_bytes);
-        tma_load_3d(st, &xmap, 0, 0, xi >> 6, xfull_bar(rp.s));  // both 64-input chunks at once
-        issued = q + 1;
+      const int n_groups = n_half / CG;
+      for (int u = 0; u < n_groups; ++u) {
+        if (u >= SU && !mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
+        const uint32_t st = smem_u32(smem + T::kXRingOff + rp.s * CG * T::kXrBytes);
+        mbar_arrive_expect_tx(xfull_bar(rp.s), 2 * CG * xr_box_bytes);
+        tma_load_3d(st, &xmap, 0, 0, cur.ub() * (UKT / 4) + h0 * 2, xfull_bar(rp.s));
+        issued = u + 1;
         rp.next();
-        if (++h == H) {
-          h = 0;
+        h0 += CG;
+        if (h0 == H) {
+          h0 = 0;
           cur.next();
-          x0 = cur.ub() * UKT * 16;
         }
       }
-      for (int q = issued - S > 0 ? issued - S : 0; q < issued; ++q) {
+      for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
         volatile int never = 0;
-        mbar_wait(xfull_bar(q % S), (q / S) & 1, &never);
+        mbar_wait(xfull_bar(u % SU), (u / SU) & 1, &never);
       }
     }
   } else if (warp >= 4 && warp < T::kProdW) {
@@ -288,11 +300,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     for (int j = 0;; ++j) {
       const int q = kWG * j + wg;
       if (q >= n_half) break;
-      bool ok = mbar_wait(wfull_bar(s), sphase, abort_flag);
+      bool ok = mbar_wait(wfull_bar(s / CG), sphase, abort_flag);
       // The A buffer: its previous half-unit's MMAs must be done.
       if (ok && j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
-      const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + s * T::kStageBytes);
+      const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + T::kWRingOff + s * T::kWBytes);
       const uint32_t a_addr = tmem + lane_off + T::kACol0 + wg * 64;
       if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(wempty_bar(s));  // the weights of this stage have been read
+        mbar_arrive(wempty_bar(s / CG));  // the weights of this stage have been read
         mbar_arrive(afull_bar(wg));
       }
       s += kWG;
@@ -338,9 +350,12 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
     const uint32_t idesc = idesc_f16_f32(128, nslots);
     // B descriptors: box 0 (k-tiles 0-3) and box 1 (4-7) of the first
     // stage's xr slice, advanced in 16-byte units.
-    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + T::kWBytes), 1024);
-    const uint64_t bdesc1 = bdesc0 + (xr_box_bytes >> 4);
-    const uint32_t stage_step = static_cast<uint32_t>(T::kStageBytes) >> 4;
+    // A group's copy lays its 2 CG chunks out back to back (nslots rows of
+    // 128 bytes each), so half-unit h of the group in slot us starts at
+    // us * CG * kXrBytes + h * 2 * xr_box_bytes of the xr ring.
+    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + T::kXRingOff), 1024);
+    const uint32_t box_step = xr_box_bytes >> 4;
+    const uint32_t unit_step = static_cast<uint32_t>(CG * T::kXrBytes) >> 4;
     bool stop = false;
     for (int sg = 0; sg < order.n_seg && !stop; ++sg) {
       const long long bb = order.block(sg);
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
           const int q = k * H + h;
           const int s = q % S;
           const int wg = q & (kWG - 1);
-          bool ok = mbar_wait(xfull_bar(s), (q / S) & 1, abort_flag);
+          bool ok = mbar_wait(xfull_bar(s / CG), (q / S) & 1, abort_flag);
           ok = ok && mbar_wait(afull_bar(wg), (q / kWG) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             stop = true;
@@ -377,8 +392,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = tmem + T::kACol0 + wg * 64;
-          const uint64_t bd0 = bdesc0 + s * stage_step;
-          const uint64_t bd1 = bdesc1 + s * stage_step;
+          const uint64_t bd0 = bdesc0 + (s / CG) * unit_step + (s % CG) * 2 * box_step;
+          const uint64_t bd1 = bd0 + box_step;
           const bool first = k == kf && h == 0;  // overwrites the accumulator
           if (elect_one()) {
             mma_f16_tmemA(d_addr, a_addr, bd0, idesc, first ? 0u : 1u);
@@ -390,7 +405,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
             mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
             mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
             mma_commit(aempty_bar(wg));
-            mma_commit(xempty_bar(s));
+            mma_commit(xempty_bar(s / CG));
           }
           __syncwarp();
         }
@@ -498,7 +513,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS>::kThreads, 1)
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
 cudaError_t tc_smem_attr() {
   static PerDeviceOnce<kMaxAttrDevices> once;
-  return smem_attr_once(once, trellis_linear_tc_kernel<BITS, LAYOUT, UKT, SLOTS>, TcCfg<BITS, SLOTS>::kBytes);
+  return smem_attr_once(once, trellis_linear_tc_kernel<BITS, LAYOUT, UKT, SLOTS>,
+                        TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kBytes);
 }
 
 // Launches the kernel of row-slot class SLOTS.
@@ -512,8 +528,8 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, const Mm
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(TcCfg<BITS, SLOTS>::kThreads);
-  cfg.dynamicSmemBytes = TcCfg<BITS, SLOTS>::kBytes;
+  cfg.blockDim = dim3(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads);
+  cfg.dynamicSmemBytes = TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -521,19 +537,22 @@ cudaError_t launch_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, const Mm
                 : cudaLaunchKernelEx(&cfg, trellis_linear_tc_kernel<BITS, kLayoutTiles, UKT, SLOTS>, wmap, xmap, p);
 }
 
-// One pass of up to 128 rows.
-template <int BITS, int UKT>
-cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
+// One pass of the row-slot class SLOTS: the tensor maps (whose boxes are
+// the class's copy groups) and the launch.
+template <int BITS, int UKT, int SLOTS>
+cudaError_t run_tc_class(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
+  constexpr int CG = TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::CG;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap wmap, xmap;
   memset(&wmap, 0, sizeof(wmap));
   if (!strips) {
-    // Packed weights as rows of u64, one row per k-tile; a box is 8 k-tiles x 8 tiles.
+    // Packed weights as rows of u64, one row per k-tile; a box is a copy
+    // group: 8 CG k-tiles x 8 tiles.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
                                 static_cast<cuuint64_t>(lp.in_features / 16)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(lp.out_features) * BITS * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(kTcHalfKt)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * BITS), static_cast<cuuint32_t>(kTcHalfKt * CG)};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint32_t*>(lp.trellis), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -542,12 +561,13 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
   }
   {
     // xr [rows][in] fp16 viewed as (64 inputs, rows, in / 64): a box of
-    // (64, the pass's row slots, 2) lands as two chunks of 64 inputs (the
-    // MMA's K-major B operand for 4 k-tiles each), each the row slots' 128-byte
-    // rows written with the 128-byte swizzle; slots past `rows` are zeros.
+    // (64, the pass's row slots, 2 CG) lands as a copy group's chunks of 64
+    // inputs (the MMA's K-major B operand for 4 k-tiles each), each the row
+    // slots' 128-byte rows written with the 128-byte swizzle; slots past
+    // `rows` are zeros.
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(lp.rows), static_cast<cuuint64_t>(lp.in_features / 64)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(lp.in_features) * 2, 128};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tc_row_slots(lp.rows)), 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(tc_row_slots(lp.rows)), static_cast<cuuint32_t>(2 * CG)};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(lp.xr), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -568,11 +588,17 @@ cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cud
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
+  return launch_tc<BITS, UKT, SLOTS>(wmap, xmap, p, strips, ws.ctas, stream);
+}
+
+// One pass of up to 128 rows.
+template <int BITS, int UKT>
+cudaError_t run_tc(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   const int ns = tc_row_slots(lp.rows);
-  if (ns <= 16) return launch_tc<BITS, UKT, 16>(wmap, xmap, p, strips, ws.ctas, stream);
-  if (ns <= 32) return launch_tc<BITS, UKT, 32>(wmap, xmap, p, strips, ws.ctas, stream);
-  if (ns <= 64) return launch_tc<BITS, UKT, 64>(wmap, xmap, p, strips, ws.ctas, stream);
-  return launch_tc<BITS, UKT, 128>(wmap, xmap, p, strips, ws.ctas, stream);
+  if (ns <= 16) return run_tc_class<BITS, UKT, 16>(lp, ws, strips, stream);
+  if (ns <= 32) return run_tc_class<BITS, UKT, 32>(lp, ws, strips, stream);
+  if (ns <= 64) return run_tc_class<BITS, UKT, 64>(lp, ws, strips, stream);
+  return run_tc_class<BITS, UKT, 128>(lp, ws, strips, stream);
 }
 
 }  // namespace
