@@ -95,18 +95,20 @@ def wait(bar, parity):
 # --------------------------------------------------------------------------
 # The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
 
-def run_tc(order, S, H, rng, ACC=2, plant=None):
+def run_tc(order, S, H, rng, ACC=2, plant=None, NB=2):
     """The tcgen05 kernel: a weights producer and an xr producer, each
     refilling its part of a unit's stages (one copy per unit of H half-units)
     once that part's readers are done (the decode warpgroups for the
     weights, the MMAs for xr); four decode warpgroups
-    (half-unit q to warpgroup q mod 4) with one A buffer each; one MMA warp per
-    chain (units at even / odd processing positions), each issuing its
+    (half-unit q to warpgroup q mod 4, two per chain, alternating on the
+    chain's half-units) sharing a ring of NB A buffers per chain; one MMA warp
+    per chain (units at even / odd processing positions), each issuing its
     chain's MMAs in order; ACC accumulator sets alternating between segments.
     `plant` names a fault to plant: "w_early" refills a stage's weights
     without waiting for the decode, "x_early" its xr slice without waiting
     for the MMAs, "no_dempty" starts a segment without waiting for the
-    readout of its accumulator set."""
+    readout of its accumulator set, "a_early" decodes into an A buffer
+    without waiting for the MMAs that read it before."""
     WG = 4
     sim = Sim(rng)
     n_half = order.n_units * H
@@ -116,13 +118,13 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
     wempty = [Bar("wempty%d" % s, 4 * CG) for s in range(SU)]
     xfull = [Bar("xfull%d" % s, 1) for s in range(SU)]
     xempty = [Bar("xempty%d" % s, CG) for s in range(SU)]
-    afull = [Bar("afull%d" % w, 4) for w in range(WG)]
-    aempty = [Bar("aempty%d" % w, 1) for w in range(WG)]
+    afull = [[Bar("afull%d.%d" % (c, b), 4) for b in range(NB)] for c in range(2)]
+    aempty = [[Bar("aempty%d.%d" % (c, b), 1) for b in range(NB)] for c in range(2)]
     dfull = [Bar("dfull%d" % d, 2) for d in range(ACC)]
     dempty = [Bar("dempty%d" % d, 4) for d in range(ACC)]
     wtag = [None] * S        # half-unit whose weights a stage holds
     xtag = [None] * S        # half-unit whose xr slice a stage holds
-    abuf = [None] * WG       # half-unit whose decoded weights an A buffer holds
+    abuf = [[None] * NB for _ in range(2)]  # half-unit whose decoded weights an A buffer holds
     acc = [[None, None] for _ in range(ACC)]  # segment whose sums a chain's accumulator holds
 
     def producer(full, empty, tag, wait_empty):
@@ -139,20 +141,25 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
             sim.copies.append(land)
 
     def decode(wg):
+        ch = (wg >> 1) if H == 2 else (wg & 1)
+        t0 = (wg & 1) if H == 2 else (wg >> 1)
         j = 0
         while WG * j + wg < n_half:
             q = WG * j + wg
             s = q % S
+            t = 2 * j + t0
+            ab = t % NB
+            assert ((q // H) & 1) == ch
             yield wait(wfull[s // CG], (q // S) & 1)
-            if j >= 1:
-                yield wait(aempty[wg], (j - 1) & 1)
+            if t >= NB and plant != "a_early":
+                yield wait(aempty[ch][ab], ((t // NB) - 1) & 1)
             assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
-            abuf[wg] = q
+            abuf[ch][ab] = q
             yield None                                    # the decode takes a while
             assert wtag[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
             for _ in range(4):
                 wempty[s // CG].arrive()
-                afull[wg].arrive()
+                afull[ch][ab].arrive()
             j += 1
 
     def segments():
@@ -173,19 +180,22 @@ def run_tc(order, S, H, rng, ACC=2, plant=None):
             for k in range(kf, P + L, 2):
                 for h in range(H):
                     q = k * H + h
-                    s, wg = q % S, q % WG
+                    s = q % S
+                    t = (k >> 1) * H + h
+                    ab = t % NB
                     assert ((q // H) & 1) == ch
                     yield wait(xfull[s // CG], (q // S) & 1)
-                    yield wait(afull[wg], (q // WG) & 1)
+                    yield wait(afull[ch][ab], (t // NB) & 1)
 
-                    def execute(q=q, s=s, wg=wg, sg=sg, d=d, first=(k == kf and h == 0)):
+                    def execute(q=q, s=s, ab=ab, sg=sg, d=d, first=(k == kf and h == 0)):
                         assert xtag[s] == q, "MMA of %d found stage %d's xr of %s" % (q, s, xtag[s])
-                        assert abuf[wg] == q, "MMA of %d found A buffer %d holding %s" % (q, wg, abuf[wg])
+                        assert abuf[ch][ab] == q, "MMA of %d found A buffer %d.%d holding %s" % (
+                            q, ch, ab, abuf[ch][ab])
                         if first:
                             acc[d][ch] = sg
                         assert acc[d][ch] == sg, "chain %d MMA of segment %d into sums of %s" % (
                             ch, sg, acc[d][ch])
-                        aempty[wg].arrive()                  # the two commits after the MMAs
+                        aempty[ch][ab].arrive()              # the two commits after the MMAs
                         xempty[s // CG].arrive()
                     sim.tensor.append(execute)
             sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
@@ -294,15 +304,16 @@ def cta_orders(seed, n):
         yield SegmentOrder(u0, u1, ub)
 
 
-@pytest.mark.parametrize("S,H,ACC", [(16, 2, 2), (12, 2, 2), (8, 2, 2), (4, 2, 1), (8, 1, 2), (4, 1, 1), (12, 1, 2)])
-def test_tc_kernel_protocol_under_random_schedules(S, H, ACC):
-    rng = random.Random(100 * S + 10 * H + ACC)
-    for order in cta_orders(S * 4 + H, 60):
+@pytest.mark.parametrize("S,H,ACC,NB", [(16, 2, 2, 3), (12, 2, 2, 3), (8, 2, 2, 2), (4, 2, 1, 2), (8, 1, 2, 3),
+                                        (4, 1, 1, 2), (12, 1, 2, 3), (16, 2, 2, 2)])
+def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, NB):
+    rng = random.Random(100 * S + 10 * H + ACC + 1000 * NB)
+    for order in cta_orders(S * 4 + H + NB, 60):
         for _ in range(3):
-            run_tc(order, S, H, rng, ACC)
+            run_tc(order, S, H, rng, ACC, NB=NB)
 
 
-@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty"])
+@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early"])
 def test_tc_planted_faults_are_caught(plant):
     """A producer that refills its part of a stage without waiting for that
     part's reader, or a chain that starts a segment in an accumulator set
@@ -312,7 +323,7 @@ def test_tc_planted_faults_are_caught(plant):
     for order in cta_orders(21, 60):
         for _ in range(5):
             try:
-                run_tc(order, 8, 2, rng, 1 if plant == "no_dempty" else 2, plant=plant)
+                run_tc(order, 8, 2, rng, 1 if plant == "no_dempty" else 2, plant=plant, NB=3)
             except AssertionError:
                 failures += 1
     assert failures > 0

@@ -103,11 +103,16 @@ struct TcCfg {
   static constexpr int kXRingOff = kStages * kWBytes;          // [kStages][kXrBytes], 1024-byte aligned
   // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
   // in kAccBufs sets that alternate between segments (so that the MMAs of a
-  // segment can start while the epilogue reads the previous one), then one
-  // A buffer of 64 columns (8 k-tiles) per decode warpgroup.
+  // segment can start while the epilogue reads the previous one), then
+  // kABufs A buffers of 64 columns (8 k-tiles) per chain, taken in turn by
+  // the chain's half-units. With two, each of the chain's two decode
+  // warpgroups (which alternate on its half-units) has one buffer of its own;
+  // a third per chain (where the columns allow) measured no faster (LM head
+  // 4 bits, 1-16 rows: 126.9 against 124.8 us).
   static constexpr int kAccBufs = SLOTS <= 64 ? 2 : 1;
+  static constexpr int kABufs = 2;
   static constexpr int kACol0 = kAccBufs * 2 * SLOTS;
-  static_assert(kACol0 + kWG * 64 <= kTcTmemCols, "Tensor Memory columns");
+  static_assert(kACol0 + 2 * kABufs * 64 <= kTcTmemCols, "Tensor Memory columns");
   // Warp roles: epilogue 0-3, decode 4-19, weights producer, xr producer,
   // and one MMA warp per chain.
   static constexpr int kProdW = 4 + 4 * kWG;
@@ -116,9 +121,9 @@ struct TcCfg {
   static constexpr int kThreads = (kMma + 2) * 32;
   static constexpr int kXchOff = kStages * kStageBytes;
   static constexpr int kBarOff = kXchOff + 8192;
-  // wfull, wempty, xfull, xempty per unit slot; afull, aempty per decode
-  // warpgroup; dfull, dempty per accumulator set; drain
-  static constexpr int kNumBars = 4 * kUnitSlots + 2 * kWG + 2 * kAccBufs + 1;
+  // wfull, wempty, xfull, xempty per unit slot; afull, aempty per A buffer;
+  // dfull, dempty per accumulator set; drain
+  static constexpr int kNumBars = 4 * kUnitSlots + 4 * kABufs + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
   static_assert(kBytes <= kSmemBudgetWide, "shared memory");
@@ -133,6 +138,18 @@ __device__ __forceinline__ void tc_decode_kt(const ColQuads<BITS>& cq, int col, 
   decode_col_words<BITS>(cw, col, a);
   tmem_st8(a_addr, a);
 }
+
+// Decodes k-tile KK of four (strips order) into registers.
+template <int BITS, int KK>
+__device__ __forceinline__ void tc_decode_kt_regs(const ColQuads<BITS>& cq, int col, uint32_t (&a)[8]) {
+  ColWords<BITS> cw;
+  quads_to_col_words<BITS, KK>(cq, cw);
+  decode_col_words<BITS>(cw, col, a);
+}
+
+// k-tiles of a half-unit a decode warp decodes before it waits for its A
+// buffer (held in 8 registers each).
+constexpr int kPreKt = 2;
 
 // The pass's row slots: `rows` rounded up to 16 (the MMA's N); slots past
 // `rows` read zeros.
@@ -176,10 +193,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   auto xfull_bar = [&](int us) { return bar0 + 8u * (2 * SU + us); };
   auto xempty_bar = [&](int us) { return bar0 + 8u * (3 * SU + us); };
   const uint32_t abar0 = bar0 + 8u * (4 * SU);
-  // The A buffer of warpgroup w; accumulator set d.
-  auto afull_bar = [&](int w) { return abar0 + 8u * w; };
-  auto aempty_bar = [&](int w) { return abar0 + 8u * (kWG + w); };
-  const uint32_t dbar0 = abar0 + 8u * (2 * kWG);
+  // A buffer b of chain ch; accumulator set d.
+  constexpr int NB = T::kABufs;
+  auto afull_bar = [&](int ch, int b) { return abar0 + 8u * (ch * NB + b); };
+  auto aempty_bar = [&](int ch, int b) { return abar0 + 8u * (2 * NB + ch * NB + b); };
+  const uint32_t dbar0 = abar0 + 8u * (4 * NB);
   auto dfull_bar = [&](int d) { return dbar0 + 8u * d; };
   auto dempty_bar = [&](int d) { return dbar0 + 8u * (kAccB + d); };
   const uint32_t drain = dbar0 + 8u * (2 * kAccB);
@@ -204,10 +222,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       mbar_init(xfull_bar(us), 1);
       mbar_init(xempty_bar(us), CG);      // the MMAs' commit, per half-unit
     }
-    for (int w = 0; w < kWG; ++w) {
-      mbar_init(afull_bar(w), 4);
-      mbar_init(aempty_bar(w), 1);
-    }
+    for (int ch = 0; ch < 2; ++ch)
+      for (int b = 0; b < NB; ++b) {
+        mbar_init(afull_bar(ch, b), 4);   // the decoding warpgroup's 4 warps
+        mbar_init(aempty_bar(ch, b), 1);  // the MMAs' commit
+      }
     for (int d = 0; d < kAccB; ++d) {
       mbar_init(dfull_bar(d), 2);  // one signal per chain
       mbar_init(dempty_bar(d), 4);
@@ -295,20 +314,52 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
     const int tile = n >> 4, col = n & 15;
+    // The warpgroup's chain (processing-position parity of its half-units'
+    // units) and its half-units' chain-local indices t0, t0 + 2, t0 + 4, ...
+    const int ch = H == 2 ? (wg >> 1) : (wg & 1);
+    const int t0 = H == 2 ? (wg & 1) : (wg >> 1);
     int s = wg;
     uint32_t sphase = 0;
     for (int j = 0;; ++j) {
       const int q = kWG * j + wg;
       if (q >= n_half) break;
+      const int t = 2 * j + t0;  // chain-local index of half-unit q
+      const int ab = t % NB;     // its A buffer; the buffer's previous user was t - NB
       bool ok = mbar_wait(wfull_bar(s / CG), sphase, abort_flag);
-      // The A buffer: its previous half-unit's MMAs must be done.
-      if (ok && j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
       const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + T::kWRingOff + s * T::kWBytes);
-      const uint32_t a_addr = tmem + lane_off + T::kACol0 + wg * 64;
+      const uint32_t a_addr = tmem + lane_off + T::kACol0 + (ch * NB + ab) * 64;
+      // The first kPreKt k-tiles are decoded into registers before the A
+      // buffer is known to be free (the MMAs of the warpgroup's previous
+      // half-unit may still be reading it), then stored once it is.
+      uint32_t pre[kPreKt][8];
       if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
-        for (int kt = 0; kt < kTcHalfKt; ++kt) {
+        for (int kt = 0; kt < kPreKt; ++kt) {
+          ColWords<BITS> cw;
+          load_col_words<BITS>(ws + (kt * 8 + tile) * 8 * BITS, col, cw);
+          decode_col_words<BITS>(cw, col, pre[kt]);
+        }
+      }
+      ColQuads<BITS> cq0;  // strips: the words of k-tiles 0-3, one 128-bit load per word
+      if constexpr (LAYOUT == kLayoutStrips) {
+        load_col_quads<BITS>(reinterpret_cast<const uint4*>(ws + tile * 32 * BITS), col, cq0);
+        tc_decode_kt_regs<BITS, 0>(cq0, col, pre[0]);
+        tc_decode_kt_regs<BITS, 1>(cq0, col, pre[1]);
+      }
+      // The A buffer: its previous half-unit's MMAs must be done.
+      // (Safe as a parity wait: this warpgroup decoded t - 2, for which it
+      // waited for the MMAs of t - 2 - NB; a chain's MMAs complete in order,
+      // so those of t - 2 NB are done, and the barrier is at most one phase
+      // behind the one waited for.)
+      if (t >= NB) ok = mbar_wait(aempty_bar(ch, ab), ((t / NB) - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kt = 0; kt < kPreKt; ++kt) tmem_st8(a_addr + kt * 8, pre[kt]);
+      if constexpr (LAYOUT == kLayoutTiles) {
+#pragma unroll
+        for (int kt = kPreKt; kt < kTcHalfKt; ++kt) {
           ColWords<BITS> cw;
           load_col_words<BITS>(ws + (kt * 8 + tile) * 8 * BITS, col, cw);
           uint32_t a[8];
@@ -316,23 +367,21 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
           tmem_st8(a_addr + kt * 8, a);
         }
       } else {
-        // Strips: one 128-bit load per word brings it for four k-tiles.
-#pragma unroll
-        for (int c4 = 0; c4 < kTcHalfKt / 4; ++c4) {
-          ColQuads<BITS> cq;
-          load_col_quads<BITS>(reinterpret_cast<const uint4*>(ws + (c4 * 8 + tile) * 32 * BITS), col, cq);
-          tc_decode_kt<BITS, 0>(cq, col, a_addr + (4 * c4 + 0) * 8);
-          tc_decode_kt<BITS, 1>(cq, col, a_addr + (4 * c4 + 1) * 8);
-          tc_decode_kt<BITS, 2>(cq, col, a_addr + (4 * c4 + 2) * 8);
-          tc_decode_kt<BITS, 3>(cq, col, a_addr + (4 * c4 + 3) * 8);
-        }
+        tc_decode_kt<BITS, 2>(cq0, col, a_addr + 2 * 8);
+        tc_decode_kt<BITS, 3>(cq0, col, a_addr + 3 * 8);
+        ColQuads<BITS> cq;
+        load_col_quads<BITS>(reinterpret_cast<const uint4*>(ws + (8 + tile) * 32 * BITS), col, cq);
+        tc_decode_kt<BITS, 0>(cq, col, a_addr + 4 * 8);
+        tc_decode_kt<BITS, 1>(cq, col, a_addr + 5 * 8);
+        tc_decode_kt<BITS, 2>(cq, col, a_addr + 6 * 8);
+        tc_decode_kt<BITS, 3>(cq, col, a_addr + 7 * 8);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(wempty_bar(s / CG));  // the weights of this stage have been read
-        mbar_arrive(afull_bar(wg));
+        mbar_arrive(afull_bar(ch, ab));
       }
       s += kWG;
       if (s >= S) {
@@ -383,15 +432,16 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
         for (int h = 0; h < H; ++h) {
           const int q = k * H + h;
           const int s = q % S;
-          const int wg = q & (kWG - 1);
+          const int t = (k >> 1) * H + h;  // chain-local index
+          const int ab = t % NB;
           bool ok = mbar_wait(xfull_bar(s / CG), (q / S) & 1, abort_flag);
-          ok = ok && mbar_wait(afull_bar(wg), (q / kWG) & 1, abort_flag);
+          ok = ok && mbar_wait(afull_bar(ch, ab), (t / NB) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = tmem + T::kACol0 + wg * 64;
+          const uint32_t a_addr = tmem + T::kACol0 + (ch * NB + ab) * 64;
           const uint64_t bd0 = bdesc0 + (s / CG) * unit_step + (s % CG) * 2 * box_step;
           const uint64_t bd1 = bd0 + box_step;
           const bool first = k == kf && h == 0;  // overwrites the accumulator
@@ -404,7 +454,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
             mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
             mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
             mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
-            mma_commit(aempty_bar(wg));
+            mma_commit(aempty_bar(ch, ab));
             mma_commit(xempty_bar(s / CG));
           }
           __syncwarp();
