@@ -314,20 +314,34 @@ def decode_rows(trellis, in_features, out_features, bits, ks):
 # outputs, stored whole; inside it, groups of four k-tiles follow in input
 # order, and a group stores its 8 n-tiles one after another with the words of
 # its four k-tiles interleaved: word w of k-tiles 4c, 4c+1, 4c+2, 4c+3 are
-# four consecutive words. Every word of the tiles appears once.
+# four consecutive words (a quad). Within an n-tile of a group the quads are
+# dealt out by w mod s, s = bits / 2 at 4 and 8 bits and 1 otherwise: quad w
+# is the (w mod s) * (8 bits / s) + w // s -th. Every word of the tiles
+# appears once.
 # ---------------------------------------------------------------------------
+def strips_quad_positions(bits):
+    """Position of quad w inside an n-tile of a group, for w = 0 .. 8 bits - 1."""
+    s = bits // 2 if bits in (4, 8) else 1
+    per = 8 * bits // s
+    return [(w % s) * per + w // s for w in range(8 * bits)]
+
+
 def tiles_to_strips(trellis, in_features, out_features, bits):
     """k-tile-major packed tiles -> strips order (same words, other order)."""
     check_shape(in_features, out_features, bits)
     kt, nt = in_features // 16, out_features // 16
     t = np.asarray(trellis, dtype=np.uint32).reshape(kt // 4, 4, nt // 8, 8, 8 * bits)
     # [group][kt%4][block][nt%8][word] -> [block][group][nt%8][word][kt%4]
-    return np.ascontiguousarray(t.transpose(2, 0, 3, 4, 1)).reshape(-1)
+    g = t.transpose(2, 0, 3, 4, 1)
+    out = np.empty_like(g)
+    out[:, :, :, strips_quad_positions(bits), :] = g
+    return np.ascontiguousarray(out).reshape(-1)
 
 
 def strips_to_tiles(strips, in_features, out_features, bits):
     check_shape(in_features, out_features, bits)
     kt, nt = in_features // 16, out_features // 16
     s = np.asarray(strips, dtype=np.uint32).reshape(nt // 8, kt // 4, 8, 8 * bits, 4)
+    s = s[:, :, :, strips_quad_positions(bits), :]   # back to word order
     # [block][group][nt%8][word][kt%4] -> [group][kt%4][block][nt%8][word]
     return np.ascontiguousarray(s.transpose(1, 4, 0, 2, 3)).reshape(-1)

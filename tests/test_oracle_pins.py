@@ -472,22 +472,32 @@ def test_decode_rows_and_blocks_agree_with_matrix():
     assert np.array_equal(bits16(o.decode_blocks(tr, 256, 256, k, [1])), bits16(w[:, 128:]))
 
 
-def test_strips_layout_places_each_word_by_hand_formula():
+@pytest.mark.parametrize("k", [3, 4, 8])
+def test_strips_layout_places_each_word_by_hand_formula(k):
     """Word w of tile (kt, nt) lands at word
-    (((b * I/64 + c) * 8 + nt % 8) * 8*bits + w) * 4 + kt % 4 of the strips
-    order, with b = nt // 8 and c = kt // 4."""
-    k, i_f, o_f = 3, 256, 384
-    tr = synth.make_trellis(i_f, o_f, k, 91)
+    (((b * I/64 + c) * 8 + nt % 8) * 8*bits + p(w)) * 4 + kt % 4 of the
+    strips order, with b = nt // 8, c = kt // 4 and p(w) = w at 3 bits,
+    p(w) = (w % 2) * 16 + w // 2 at 4 bits (written out below) and
+    (w % 4) * 16 + w // 4 at 8 bits."""
+    i_f, o_f = 256, 384
+    tr = synth.make_trellis(i_f, o_f, k, 91 + k)
     st = o.tiles_to_strips(tr, i_f, o_f, k)
     per = 8 * k
     groups = i_f // 64
+    if k == 4:   # even words first, then odd ones
+        pos = {w: (w // 2 if w % 2 == 0 else 16 + w // 2) for w in range(per)}
+    elif k == 8:
+        pos = {w: (w % 4) * 16 + w // 4 for w in range(per)}
+    else:
+        pos = {w: w for w in range(per)}
+    assert sorted(pos.values()) == list(range(per))
     seen = np.zeros(st.size, dtype=bool)
     for kt in range(i_f // 16):
         for nt in range(o_f // 16):
             b, c = nt // 8, kt // 4
             for w in range(per):
                 src = (kt * (o_f // 16) + nt) * per + w
-                dst = (((b * groups + c) * 8 + nt % 8) * per + w) * 4 + kt % 4
+                dst = (((b * groups + c) * 8 + nt % 8) * per + pos[w]) * 4 + kt % 4
                 assert st[dst] == tr[src]
                 seen[dst] = True
     assert seen.all()

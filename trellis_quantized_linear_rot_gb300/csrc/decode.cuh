@@ -223,23 +223,6 @@ __device__ __forceinline__ void load_group4(const uint32_t* tw, const Group4Pos<
   if constexpr (Group4<BITS>::kWords == 3) gw.x[2] = tw[q.w2];
 }
 
-// Interleaved form (the strips order): the words of four consecutive k-tiles
-// are stored together, word w of k-tiles 4c .. 4c+3 forming one 16-byte
-// chunk, so one 128-bit load brings a word for four k-tiles.
-template <int BITS>
-struct Group4Quads {
-  uint4 q[Group4<BITS>::kWords];
-};
-
-// `tq` points at the tile's chunks for one group of four k-tiles.
-template <int BITS>
-__device__ __forceinline__ void load_group4_quads(const uint4* tq, const Group4Pos<BITS>& p,
-                                                  Group4Quads<BITS>& gq) {
-  gq.q[0] = tq[p.w0];
-  gq.q[1] = tq[p.w1];
-  if constexpr (Group4<BITS>::kWords == 3) gq.q[2] = tq[p.w2];
-}
-
 template <int KK>
 __device__ __forceinline__ uint32_t quad_word(const uint4& v) {
   if constexpr (KK == 0) return v.x;
@@ -248,16 +231,32 @@ __device__ __forceinline__ uint32_t quad_word(const uint4& v) {
   return v.w;
 }
 
-// The words of k-tile KK (0..3) of the group.
-template <int BITS, int KK>
-__device__ __forceinline__ void quads_to_words(const Group4Quads<BITS>& gq, Group4Words<BITS>& gw) {
-#pragma unroll
-  for (int i = 0; i < Group4<BITS>::kWords; ++i) gw.x[i] = quad_word<KK>(gq.q[i]);
+// The strips order keeps, for each tile and group of four consecutive
+// k-tiles, the tile's 8 * bits word quads (word w of the four k-tiles, 16
+// bytes) together, in an order chosen so that the 16 threads that decode the
+// tile's columns read them with 128-bit shared-memory loads free of bank
+// conflicts. A thread's i-th word of a group is word (row_first_bit(n) / 32 +
+// i) mod 8 bits; at 4 and 8 bits these start every s = bits / 2 words, so
+// the quads are dealt out by w mod s: quad w sits at position
+// (w mod s) * (8 bits / s) + w / s, which makes the threads' i-th quads
+// consecutive. The other widths keep the plain order (at 2 and 6 bits the
+// threads' quads already fall in distinct banks; at 3 and 5 bits two
+// threads of eight share a bank).
+__host__ __device__ constexpr int strips_quad_spread(int bits) { return (bits == 4 || bits == 8) ? bits / 2 : 1; }
+
+__host__ __device__ constexpr int strips_quad_pos(int bits, int w) {
+  return (w % strips_quad_spread(bits)) * (8 * bits / strips_quad_spread(bits)) + w / strips_quad_spread(bits);
 }
 
-// Column form over the strips order: the words column n needs for four
-// consecutive k-tiles (word w of k-tile kk at 4w + kk), one 128-bit load per
-// word, then k-tile KK's words out of them.
+// The word held at position `pos` (the inverse of strips_quad_pos).
+__host__ __device__ constexpr int strips_quad_word(int bits, int pos) {
+  return (pos % (8 * bits / strips_quad_spread(bits))) * strips_quad_spread(bits) +
+         pos / (8 * bits / strips_quad_spread(bits));
+}
+
+// Column form over the strips order: the word quads column n needs for four
+// consecutive k-tiles, one 128-bit load each, then k-tile KK's words out of
+// them.
 template <int BITS>
 struct ColQuads {
   uint4 q[ColWords<BITS>::kCount];
@@ -266,13 +265,13 @@ struct ColQuads {
 template <int BITS>
 __device__ __forceinline__ void load_col_quads(const uint4* tq, int n, ColQuads<BITS>& cq) {
   if constexpr (BITS == 4) {
-    cq.q[0] = tq[(2 * n + 31) & 31];
-    cq.q[1] = tq[2 * n];
-    cq.q[2] = tq[2 * n + 1];
+    cq.q[0] = tq[16 + ((n + 15) & 15)];  // word 2n - 1 (mod 32)
+    cq.q[1] = tq[n];                     // word 2n
+    cq.q[2] = tq[16 + n];                // word 2n + 1
   } else if constexpr (BITS == 8) {
-    cq.q[0] = tq[(4 * n + 63) & 63];
+    cq.q[0] = tq[48 + ((n + 15) & 15)];  // word 4n - 1 (mod 64)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) cq.q[1 + j] = tq[4 * n + j];
+    for (int j = 0; j < 4; ++j) cq.q[1 + j] = tq[16 * j + n];  // word 4n + j
   } else {
     using S = RowSpan<BITS>;
     const int w0 = row_first_bit<BITS>(n) >> 5;

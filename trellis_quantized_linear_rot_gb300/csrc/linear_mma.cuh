@@ -217,57 +217,17 @@ __device__ __forceinline__ void load_b(const uint8_t* x, uint2 (&b)[NB]) {
   for (int q = 0; q < NB; ++q) b[q] = *reinterpret_cast<const uint2*>(x + q * 1024);
 }
 
-template <int BITS, int NB, int KK>
-__device__ __forceinline__ void quad_step(const Group4Quads<BITS>& qa, const Group4Quads<BITS>& qb,
-                                          const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
-                                          const uint8_t* xg, const int (&xoff)[4], float (&d)[NB][4]) {
-  Group4Words<BITS> wa, wb;
-  quads_to_words<BITS, KK>(qa, wa);
-  quads_to_words<BITS, KK>(qb, wb);
-  uint2 b[NB];
-  load_b<NB>(xg + xoff[KK], b);
-  tile_step<BITS, NB>(wa, wb, pos_a, pos_b, b, d);
-}
-
-// A unit in the strips order: `tq` is the warp's tile in the first group of
-// four k-tiles (chunk (c, tile, word) at (c * 8 + tile) * 8 * bits + word);
-// one 128-bit load per word brings it for four k-tiles, and the next group's
-// chunks are loaded while the current group is decoded.
-template <int BITS, int NB, int UKT>
-__device__ __forceinline__ void strips_unit(const uint4* tq, const uint8_t* xs, const int (&xoff)[4],
-                                            const Group4Pos<BITS>& pos_a, const Group4Pos<BITS>& pos_b,
-                                            float (&d)[NB][4]) {
-  constexpr int kChunk = 128 * Slots<NB>::kRows;
-  Group4Quads<BITS> qa, qb;
-  load_group4_quads<BITS>(tq, pos_a, qa);
-  load_group4_quads<BITS>(tq, pos_b, qb);
-#pragma unroll
-  for (int c = 0; c < UKT / 4; ++c) {
-    Group4Quads<BITS> na, nb;
-    if (c + 1 < UKT / 4) {
-      load_group4_quads<BITS>(tq + (c + 1) * 64 * BITS, pos_a, na);
-      load_group4_quads<BITS>(tq + (c + 1) * 64 * BITS, pos_b, nb);
-    }
-    const uint8_t* xg = xs + c * kChunk;
-    quad_step<BITS, NB, 0>(qa, qb, pos_a, pos_b, xg, xoff, d);
-    quad_step<BITS, NB, 1>(qa, qb, pos_a, pos_b, xg, xoff, d);
-    quad_step<BITS, NB, 2>(qa, qb, pos_a, pos_b, xg, xoff, d);
-    quad_step<BITS, NB, 3>(qa, qb, pos_a, pos_b, xg, xoff, d);
-    if (c + 1 < UKT / 4) {
-      qa = na;
-      qb = nb;
-    }
-  }
-}
-
 // Weight layouts: k-tile major ("tiles": tile (kt, nt) at (kt*O/16 + nt)),
 // landing in shared memory as [k-tile][8 tiles][words]; or block-contiguous
 // with the words of four consecutive k-tiles interleaved ("strips": block b,
-// then groups of four k-tiles, then [tile % 8][word][k-tile % 4]), landing as
-// [k-tile / 4][8 tiles][words][k-tile % 4].
+// then groups of four k-tiles, then [tile % 8][word quad][k-tile % 4], the
+// quads in the order strips_quad_pos gives), landing as
+// [k-tile / 4][8 tiles][word quads][k-tile % 4]. This kernel reads the
+// tiles order (the no-allocation entry point's); the strips order is the
+// tcgen05 kernel's.
 enum { kLayoutTiles = 0, kLayoutStrips = 1 };
 
-template <int BITS, int NB, int LAYOUT, int UKT>
+template <int BITS, int NB, int UKT>
 __global__ void __launch_bounds__(kThreads, 1)
     trellis_linear_mma_kernel(const __grid_constant__ CUtensorMap wmap,
                               const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
@@ -316,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == kProducerWarp && lane == 0) {
-    if (LAYOUT == kLayoutTiles) tma_prefetch_desc(&wmap);
+    tma_prefetch_desc(&wmap);
     tma_prefetch_desc(&xmap);
   }
   __syncthreads();
@@ -335,11 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < pre; ++i) {
         const uint32_t st = smem_u32(smem + i * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(i), L::kStageBytes);
-        if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(i));
-        else
-          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * C::kWUnitBytes, C::kWUnitBytes,
-                       full_bar(i));
+        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(i));
         cur.next();
       }
       pdl_wait_prerequisites();
@@ -355,11 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (round > 0 && !mbar_wait_sleepy(empty_bar(s), (round - 1) & 1, abort_flag, 128)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
-        if (LAYOUT == kLayoutTiles)
-          tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(s));
-        else
-          bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * C::kWUnitBytes, C::kWUnitBytes,
-                       full_bar(s));
+        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(s));
         tma_load_3d(st + C::kWUnitBytes, &xmap, 0, 0, cur.ub() * (UKT / 4), full_bar(s));
         issued = i + 1;
         cur.next();
@@ -411,13 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint8_t* st = smem + s * L::kStageBytes;
         const uint8_t* xs = st + C::kWUnitBytes;
-        if constexpr (LAYOUT == kLayoutStrips) {
-          strips_unit<BITS, NB, UKT>(reinterpret_cast<const uint4*>(st) + j * 8 * BITS, xs, xoff, pos_a, pos_b,
-                                      d);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty_bar(s));
-          continue;
-        }
         const uint32_t* wtile = reinterpret_cast<const uint32_t*>(st + j * 32 * BITS);
         // Software pipeline over k-tiles: the words and B fragments of tile
         // kt + 1 are loaded before tile kt is decoded.
@@ -469,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue
+    pdl_wait_prerequisites();  // partial sums, counters and y follow the kernel before
     const int t = threadIdx.x;  // output within the block
     LinearPass lp;
     lp.svh = p.svh;
@@ -568,16 +514,16 @@ cudaError_t smem_attr_once(PerDeviceOnce<kMaxAttrDevices>& once, Kernel kernel, 
   }));
 }
 
-template <int BITS, int NB, int LAYOUT, int UKT>
+template <int BITS, int NB, int UKT>
 cudaError_t set_smem_attr() {
   static PerDeviceOnce<kMaxAttrDevices> once;
-  return smem_attr_once(once, trellis_linear_mma_kernel<BITS, NB, LAYOUT, UKT>, Layout<BITS, UKT, NB>::kBytes);
+  return smem_attr_once(once, trellis_linear_mma_kernel<BITS, NB, UKT>, Layout<BITS, UKT, NB>::kBytes);
 }
 
-template <int BITS, int NB, int LAYOUT, int UKT>
+template <int BITS, int NB, int UKT>
 cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
                        cudaStream_t stream) {
-  cudaError_t e = set_smem_attr<BITS, NB, LAYOUT, UKT>();
+  cudaError_t e = set_smem_attr<BITS, NB, UKT>();
   if (e != cudaSuccess) return e;
   // Programmatic stream serialisation: this kernel may start while the
   // kernel before it (the input rotation) finishes; its producer waits for
@@ -592,23 +538,17 @@ cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const M
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, trellis_linear_mma_kernel<BITS, NB, LAYOUT, UKT>, wmap, xmap, p);
+  return cudaLaunchKernelEx(&cfg, trellis_linear_mma_kernel<BITS, NB, UKT>, wmap, xmap, p);
 }
 
-template <int BITS, int LAYOUT, int UKT>
-cudaError_t launch_mma(const CUtensorMap& wmap, const CUtensorMap& xmap, const MmaParams& p, int ctas,
-                       cudaStream_t stream) {
-  if (p.rows > 8) return launch_one<BITS, 2, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
-  return launch_one<BITS, 1, LAYOUT, UKT>(wmap, xmap, p, ctas, stream);
-}
-
+// One pass of up to 16 rows on weights in the tiles order.
 template <int BITS, int UKT>
 cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
+  if (strips) return cudaErrorInvalidValue;  // the tcgen05 kernel's order
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap wmap, xmap;
-  memset(&wmap, 0, sizeof(wmap));
-  if (!strips) {
+  {
     // Packed weights as rows of u64: one row per k-tile, O * BITS / 4 words.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(lp.out_features) * BITS / 4,
                                 static_cast<cuuint64_t>(lp.in_features / 16)};
@@ -636,7 +576,7 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
       return cudaErrorInvalidValue;
   }
   MmaParams p;
-  p.strips = reinterpret_cast<const uint8_t*>(lp.trellis);
+  p.strips = nullptr;
   p.svh = lp.svh;
   p.y = lp.y;
   p.partials = ws.partials;
@@ -649,8 +589,8 @@ cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cu
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
-  return strips ? launch_mma<BITS, kLayoutStrips, UKT>(wmap, xmap, p, ws.ctas, stream)
-                : launch_mma<BITS, kLayoutTiles, UKT>(wmap, xmap, p, ws.ctas, stream);
+  if (p.rows > 8) return launch_one<BITS, 2, UKT>(wmap, xmap, p, ws.ctas, stream);
+  return launch_one<BITS, 1, UKT>(wmap, xmap, p, ws.ctas, stream);
 }
 
 }  // namespace

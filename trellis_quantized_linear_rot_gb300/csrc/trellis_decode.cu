@@ -37,18 +37,20 @@ __global__ void __launch_bounds__(128) trellis_decode_kernel(const uint32_t* __r
 
 // Tiles -> strips: one 16-byte chunk of the strips order per thread.
 // Strips order: block b of 128 outputs, then group c of four k-tiles, then
-// [n-tile % 8][word w][k-tile % 4]; chunk (b, c, nn, w) holds word w of the
-// tiles (4c + kk, 8b + nn), kk = 0..3. The four words come from four k-tile
-// rows of the tiles order; consecutive threads read consecutive words of one
-// tile, so each of the four loads is coalesced.
+// [n-tile % 8][position][k-tile % 4]; chunk (b, c, nn, position) holds word
+// w = strips_quad_word(bits, position) of the tiles (4c + kk, 8b + nn),
+// kk = 0..3. The four words come from four k-tile rows of the tiles order;
+// consecutive threads read words of one tile a few words apart, so the loads
+// stay within a few sectors.
 __global__ void __launch_bounds__(256) tiles_to_strips_kernel(const uint32_t* __restrict__ tiles,
                                                               uint4* __restrict__ strips,
-                                                              long long chunks, int tile_words,
+                                                              long long chunks, int bits,
                                                               int groups_per_block, int n_tiles) {
+  const int tile_words = 8 * bits;
   const long long row_words = static_cast<long long>(n_tiles) * tile_words;  // one k-tile row
   for (long long q = blockIdx.x * 256LL + threadIdx.x; q < chunks; q += static_cast<long long>(gridDim.x) * 256) {
     const long long tq = q / tile_words;  // (b, c, nn)
-    const int w = static_cast<int>(q - tq * tile_words);
+    const int w = strips_quad_word(bits, static_cast<int>(q - tq * tile_words));
     const int nn = static_cast<int>(tq & 7);
     const long long bc = tq >> 3;         // b * groups_per_block + c
     const long long b = bc / groups_per_block;
@@ -96,7 +98,7 @@ cudaError_t launch_tiles_to_strips(const uint32_t* tiles, uint32_t* strips, int 
   long long grid = (chunks + 255) / 256;
   if (grid > 152LL * 16) grid = 152LL * 16;
   tiles_to_strips_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      tiles, reinterpret_cast<uint4*>(strips), chunks, tile_words, in_features / 64, out_features / 16);
+      tiles, reinterpret_cast<uint4*>(strips), chunks, bits, in_features / 64, out_features / 16);
   return cudaGetLastError();
 }
 
