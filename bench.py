@@ -494,6 +494,15 @@ def run_ours(args):
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        # Untimed steps for --load-s seconds first, so that the clock samples
+        # (every 20 ms) see the GPU under this load even when the timed
+        # region itself is a few milliseconds.
+        t_load = time.perf_counter()
+        while time.perf_counter() - t_load < args.load_s:
+            for _ in range(16):
+                step(False)
+            torch.cuda.synchronize()
+        barrier()
         start.record(stream)
         for _ in range(args.steps):
             step(True)
@@ -617,6 +626,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations")
     ap.add_argument("--config-iters", type=int, default=20)
+    ap.add_argument("--load-s", type=float, default=0.5,
+                    help="untimed steps run under the clock sampler before the timed region (seconds)")
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
     ap.add_argument("--layout", choices=["tiles", "strips"], default="strips",
                     help="weight storage order: strips (repacked once at load, untimed; the default) "
