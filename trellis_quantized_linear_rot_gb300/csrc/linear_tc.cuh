@@ -498,6 +498,22 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       const bool shared = c_first != c_last;
       const int slot = shared ? partial_slot(c, b, p) : 2;
       float* mine = p.partials + (static_cast<size_t>(c) * kTcPartialSlots + slot) * slot_floats;
+      if (SLOTS == 16 && !shared) {
+        // A block this CTA owns, in a pass of up to 16 rows: the two chains'
+        // sum stays in registers, and only the pass's rows are rotated.
+        float g0[16], g1[16], v[16];
+        tmem_ld16(tmem + lane_off + (dset * 2) * SLOTS, g0);
+        tmem_ld16(tmem + lane_off + (dset * 2 + 1) * SLOTS, g1);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dempty_bar(dset));  // the MMA warp may reuse the set
+        fwht_outputs(v, p.rows, t, xch, 1, 128);
+        store_outputs(v, lp, b, t, 0);
+        group_sync(1, 128);
+        continue;
+      }
       // The two chains' sums, added in chain order, into this CTA's slot.
 #pragma unroll 1
       for (int r0 = 0; r0 < p.rows; r0 += 16) {
