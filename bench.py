@@ -7,9 +7,9 @@ rows", section "What this changes": x ~ N(0,1) fp16, suh/svh random sign *
 U[0.5,1.5], uniformly random packed trellis bits).
 
 A step is the whole hot path for each row count: tf_rot_in then the trellis
-linear. The weights are stored in the library's strips order (repacked once
-from the k-tile-major tiles at load time, outside the timed region;
-`--layout tiles` times the k-tile-major order instead). The packed weights
+linear. The weights are in the k-tile-major order of the packed tiles
+(`--layout strips` times the library's strips order instead, repacked once
+at load time, outside the timed region). The packed weights
 (331 MB each) exceed the 129 MB L2; two copies alternate between calls, so no
 call finds its weights in L2.
 
@@ -629,9 +629,9 @@ def main():
     ap.add_argument("--load-s", type=float, default=0.5,
                     help="untimed steps run under the clock sampler before the timed region (seconds)")
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
-    ap.add_argument("--layout", choices=["tiles", "strips"], default="strips",
-                    help="weight storage order: strips (repacked once at load, untimed; the default) "
-                         "or the k-tile-major tiles")
+    ap.add_argument("--layout", choices=["tiles", "strips"], default="tiles",
+                    help="weight storage order: the k-tile-major tiles (the default) or strips "
+                         "(repacked once at load, untimed)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

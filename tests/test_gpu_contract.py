@@ -52,30 +52,35 @@ def block_cols(blocks):
 
 # ------------------------------------------------- the benchmark's own launch
 @pytest.fixture(scope="module")
-def head_strips():
-    """The benchmark's workload: LM head 5120 -> 129,280 at 4 bits in the
-    strips order, fp32 logits; the oracle's weights of the first, second and
-    last blocks and of every block the launch cuts between CTAs."""
+def head():
+    """The benchmark's workload: LM head 5120 -> 129,280 at 4 bits, fp32
+    logits, the weights in both orders (the k-tile order the benchmark times
+    by default, and the strips order of its --layout strips); the oracle's
+    weights of the first, second and last blocks and of every block the
+    launch cuts between CTAs."""
     i_f, o_f, bits = 5120, 129280, 4
     x, suh, svh, tr = inputs(16, i_f, o_f, bits, c=2)
     blocks = sorted({0, 1, o_f // 128 - 1} | set(cut_blocks(num_sms(), i_f, o_f, bits)))
     w = o.decode_blocks(tr, i_f, o_f, bits, blocks)
-    tr_t = tf.tf_trellis_to_strips(dev(tr), i_f, o_f, bits)
-    return dict(i_f=i_f, o_f=o_f, bits=bits, x=x, suh=suh, svh=svh, tr_t=tr_t, blocks=blocks, w=w)
+    tiles_t = dev(tr)
+    strips_t = tf.tf_trellis_to_strips(tiles_t, i_f, o_f, bits)
+    return dict(i_f=i_f, o_f=o_f, bits=bits, x=x, suh=suh, svh=svh, tiles=tiles_t, strips=strips_t,
+                blocks=blocks, w=w)
 
 
+@pytest.mark.parametrize("layout", ["tiles", "strips"])
 @pytest.mark.parametrize("rows", [1, 8, 16])
-def test_benchmark_launch_matches_oracle_at_every_cut_block(head_strips, rows):
-    """rot_in then tf_trellis_linear_strips exactly as the benchmark launches
-    them (same shape, weight order, output dtype and CTA count), compared
-    with the float64 oracle element by element on the blocks whose sums are
-    split between CTAs (the cross-CTA partial-sum path), and the first and
-    last blocks; every output is finite."""
-    h = head_strips
+def test_benchmark_launch_matches_oracle_at_every_cut_block(head, rows, layout):
+    """rot_in then the linear exactly as the benchmark launches them (same
+    shape, weight order, output dtype and CTA count), compared with the
+    float64 oracle element by element on the blocks whose sums are split
+    between CTAs (the cross-CTA partial-sum path), and the first and last
+    blocks; every output is finite."""
+    h = head
     assert len(h["blocks"]) > 100
     xr_t = tf.tf_rot_in(dev(h["x"][:rows]), dev(h["suh"]))
-    y = host(tf.tf_trellis_linear_strips(xr_t, h["tr_t"], dev(h["svh"]), h["bits"], h["o_f"],
-                                         out_dtype=torch.float32))
+    linear = tf.tf_trellis_linear if layout == "tiles" else tf.tf_trellis_linear_strips
+    y = host(linear(xr_t, h[layout], dev(h["svh"]), h["bits"], h["o_f"], out_dtype=torch.float32))
     tf.tf_device_error()
     assert np.all(np.isfinite(y))
     cols = block_cols(h["blocks"])
