@@ -280,6 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&xmap);
   }
   __syncthreads();
+  // The kernel after this one may be scheduled now; it waits for this one
+  // before touching memory this one reads or writes (as this one does for
+  // the kernel before it).
+  pdl_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer

@@ -55,11 +55,12 @@
 // the thread's own chain of dependent instructions), so the two producers
 // keep their loops short and work from counters, not divisions.
 //
-// Ordering with the kernel before this one (programmatic dependent launch):
-// every thread that reads memory that kernel may write (xr, by the xr
+// Ordering with the kernels around this one (programmatic dependent launch):
+// every thread that reads memory the kernel before may write (xr, by the xr
 // producer's copies) or touches the partial sums, counters or y (the
 // epilogue) first executes griddepcontrol.wait; the weight copies and the
-// decode may run before it.
+// decode may run before it. The kernel lets the next one be scheduled as
+// soon as it starts, since that one waits in the same way.
 // All waits are bounded; a kernel that gives up sets the error flag and exits.
 #pragma once
 
@@ -244,6 +245,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // The kernel after this one may be scheduled now: every kernel of this
+  // library waits (griddepcontrol.wait) for this one before it touches
+  // memory this one reads or writes, and only the weights, which no kernel
+  // writes, are read before that wait.
+  pdl_launch_dependents();
 
   if (warp == T::kProdW) {
     // ---------------------------------------------------- weights producer

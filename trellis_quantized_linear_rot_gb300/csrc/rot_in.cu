@@ -58,6 +58,10 @@ __global__ void __launch_bounds__(256) rot_in_kernel(const void* __restrict__ x,
   // The linear that follows may start its prologue (its weight copies need
   // nothing from this kernel); it waits for xr before reading it.
   pdl_launch_dependents();
+  // This kernel itself may have started before the kernel before it (a
+  // linear still reading an xr this call overwrites, or whatever wrote x)
+  // has finished: wait for it before touching memory.
+  pdl_wait_prerequisites();
   const int lane = threadIdx.x & 31;
   const int warps_per_cta = blockDim.x >> 5;
   const int blocks_per_row = in_features >> 7;
@@ -112,13 +116,24 @@ cudaError_t launch_rot_in(const void* x, int x_dtype, const __half* suh, __half*
   const long long cap = static_cast<long long>(num_sms) * 8;
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
-  const dim3 grid(static_cast<unsigned>(ctas)), block(warps * 32);
+  // Programmatic stream serialisation: the launch may be processed while
+  // the kernel before it finishes; the kernel waits for it before touching
+  // memory.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(warps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (x_dtype) {
-    case 0: rot_in_kernel<0><<<grid, block, 0, stream>>>(x, suh, xr, rows, in_features); break;
-    case 1: rot_in_kernel<1><<<grid, block, 0, stream>>>(x, suh, xr, rows, in_features); break;
-    default: rot_in_kernel<2><<<grid, block, 0, stream>>>(x, suh, xr, rows, in_features); break;
+    case 0: return cudaLaunchKernelEx(&cfg, rot_in_kernel<0>, x, suh, xr, rows, in_features);
+    case 1: return cudaLaunchKernelEx(&cfg, rot_in_kernel<1>, x, suh, xr, rows, in_features);
+    default: return cudaLaunchKernelEx(&cfg, rot_in_kernel<2>, x, suh, xr, rows, in_features);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace tfx
