@@ -95,36 +95,38 @@ def wait(bar, parity):
 # --------------------------------------------------------------------------
 # The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
 
-def run_tc(order, S, H, rng, ACC=2, plant=None, NB=2):
+def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
     """The tcgen05 kernel: a weights producer and an xr producer, each
-    refilling its part of a unit's stages (one copy per unit of H half-units)
-    once that part's readers are done (the decode warpgroups for the
-    weights, the MMAs for xr); four decode warpgroups
-    (half-unit q to warpgroup q mod 4, two per chain, alternating on the
-    chain's half-units) sharing a ring of NB A buffers per chain; one MMA warp
-    per chain (units at even / odd processing positions), each issuing its
-    chain's MMAs in order; ACC accumulator sets alternating between segments.
+    refilling its part of a unit's stages (one copy per unit of H half-units
+    where the ring allows) once that part's readers are done (the decode
+    warpgroups for the weights, the MMAs for xr); WG decode warpgroups
+    (half-unit q to warpgroup q mod WG), each with one A buffer whose uses
+    go to whichever chain the half-unit belongs to, signalled through four
+    full barriers (use j on barrier j mod 4); one MMA warp per chain (units
+    at even / odd processing positions), each issuing its chain's MMAs in
+    order; ACC accumulator sets alternating between segments.
     `plant` names a fault to plant: "w_early" refills a stage's weights
     without waiting for the decode, "x_early" its xr slice without waiting
     for the MMAs, "no_dempty" starts a segment without waiting for the
     readout of its accumulator set, "a_early" decodes into an A buffer
-    without waiting for the MMAs that read it before."""
-    WG = 4
+    without waiting for the MMAs that read it before, "one_afull" signals
+    every use of an A buffer on a single full barrier."""
     sim = Sim(rng)
     n_half = order.n_units * H
-    CG = H if S >= 8 else 1  # half-units per copy: a unit where the ring is deep enough
+    CG = H if (S >= 8 and S % (WG * H // (H if WG % H == 0 else 1)) == 0) else 1
     SU = S // CG             # copy slots: the barriers go by copies
     wfull = [Bar("wfull%d" % s, 1) for s in range(SU)]
     wempty = [Bar("wempty%d" % s, 4 * CG) for s in range(SU)]
     xfull = [Bar("xfull%d" % s, 1) for s in range(SU)]
     xempty = [Bar("xempty%d" % s, CG) for s in range(SU)]
-    afull = [[Bar("afull%d.%d" % (c, b), 4) for b in range(NB)] for c in range(2)]
-    aempty = [[Bar("aempty%d.%d" % (c, b), 1) for b in range(NB)] for c in range(2)]
+    AF = 1 if plant == "one_afull" else 4  # full barriers per warpgroup: use j on barrier j % AF
+    afull = [[Bar("afull%d.%d" % (g, b), 4) for b in range(AF)] for g in range(WG)]
+    aempty = [Bar("aempty%d" % g, 1) for g in range(WG)]
     dfull = [Bar("dfull%d" % d, 2) for d in range(ACC)]
     dempty = [Bar("dempty%d" % d, 4) for d in range(ACC)]
     wtag = [None] * S        # half-unit whose weights a stage holds
     xtag = [None] * S        # half-unit whose xr slice a stage holds
-    abuf = [[None] * NB for _ in range(2)]  # half-unit whose decoded weights an A buffer holds
+    abuf = [None] * WG  # half-unit whose decoded weights a warpgroup's A buffer holds
     acc = [[None, None] for _ in range(ACC)]  # segment whose sums a chain's accumulator holds
 
     def producer(full, empty, tag, wait_empty):
@@ -141,25 +143,20 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, NB=2):
             sim.copies.append(land)
 
     def decode(wg):
-        ch = (wg >> 1) if H == 2 else (wg & 1)
-        t0 = (wg & 1) if H == 2 else (wg >> 1)
         j = 0
         while WG * j + wg < n_half:
             q = WG * j + wg
             s = q % S
-            t = 2 * j + t0
-            ab = t % NB
-            assert ((q // H) & 1) == ch
             yield wait(wfull[s // CG], (q // S) & 1)
-            if t >= NB and plant != "a_early":
-                yield wait(aempty[ch][ab], ((t // NB) - 1) & 1)
+            if j >= 1 and plant != "a_early":
+                yield wait(aempty[wg], (j - 1) & 1)
             assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
-            abuf[ch][ab] = q
+            abuf[wg] = q
             yield None                                    # the decode takes a while
             assert wtag[s] == q, "stage %d refilled while half-unit %d was decoded" % (s, q)
             for _ in range(4):
                 wempty[s // CG].arrive()
-                afull[ch][ab].arrive()
+                afull[wg][j % AF].arrive()
             j += 1
 
     def segments():
@@ -181,21 +178,20 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, NB=2):
                 for h in range(H):
                     q = k * H + h
                     s = q % S
-                    t = (k >> 1) * H + h
-                    ab = t % NB
+                    g = q % WG
                     assert ((q // H) & 1) == ch
                     yield wait(xfull[s // CG], (q // S) & 1)
-                    yield wait(afull[ch][ab], (t // NB) & 1)
+                    jj = q // WG
+                    yield wait(afull[g][jj % AF], (jj // AF) & 1)
 
-                    def execute(q=q, s=s, ab=ab, sg=sg, d=d, first=(k == kf and h == 0)):
+                    def execute(q=q, s=s, g=g, sg=sg, d=d, first=(k == kf and h == 0)):
                         assert xtag[s] == q, "MMA of %d found stage %d's xr of %s" % (q, s, xtag[s])
-                        assert abuf[ch][ab] == q, "MMA of %d found A buffer %d.%d holding %s" % (
-                            q, ch, ab, abuf[ch][ab])
+                        assert abuf[g] == q, "MMA of %d found A buffer %d holding %s" % (q, g, abuf[g])
                         if first:
                             acc[d][ch] = sg
                         assert acc[d][ch] == sg, "chain %d MMA of segment %d into sums of %s" % (
                             ch, sg, acc[d][ch])
-                        aempty[ch][ab].arrive()              # the two commits after the MMAs
+                        aempty[g].arrive()                   # the two commits after the MMAs
                         xempty[s // CG].arrive()
                     sim.tensor.append(execute)
             sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
@@ -304,16 +300,19 @@ def cta_orders(seed, n):
         yield SegmentOrder(u0, u1, ub)
 
 
-@pytest.mark.parametrize("S,H,ACC,NB", [(16, 2, 2, 3), (12, 2, 2, 3), (8, 2, 2, 2), (4, 2, 1, 2), (8, 1, 2, 3),
-                                        (4, 1, 1, 2), (12, 1, 2, 3), (16, 2, 2, 2)])
-def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, NB):
-    rng = random.Random(100 * S + 10 * H + ACC + 1000 * NB)
-    for order in cta_orders(S * 4 + H + NB, 60):
+# (stages, half-units per unit, accumulator sets, decode warpgroups): the
+# kernel's row-slot classes (five warpgroups up to 32 row slots: 10 stages,
+# or 15 at one half-unit per unit; four beyond: 8 and 4 stages) and others.
+@pytest.mark.parametrize("S,H,ACC,WG", [(10, 2, 2, 5), (15, 1, 2, 5), (8, 2, 2, 4), (4, 2, 1, 4), (16, 2, 2, 4),
+                                        (12, 2, 2, 4), (8, 1, 2, 4), (4, 1, 1, 4), (20, 2, 2, 5)])
+def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, WG):
+    rng = random.Random(100 * S + 10 * H + ACC + 1000 * WG)
+    for order in cta_orders(S * 4 + H + WG, 60):
         for _ in range(3):
-            run_tc(order, S, H, rng, ACC, NB=NB)
+            run_tc(order, S, H, rng, ACC, WG=WG)
 
 
-@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early"])
+@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early", "one_afull"])
 def test_tc_planted_faults_are_caught(plant):
     """A producer that refills its part of a stage without waiting for that
     part's reader, or a chain that starts a segment in an accumulator set
@@ -323,7 +322,7 @@ def test_tc_planted_faults_are_caught(plant):
     for order in cta_orders(21, 60):
         for _ in range(5):
             try:
-                run_tc(order, 8, 2, rng, 1 if plant == "no_dempty" else 2, plant=plant, NB=3)
+                run_tc(order, 10, 2, rng, 1 if plant == "no_dempty" else 2, plant=plant, WG=5)
             except AssertionError:
                 failures += 1
     assert failures > 0
@@ -338,16 +337,15 @@ def test_mma_kernel_protocol_under_random_schedules(S):
 
 
 def test_planted_fault_is_caught():
-    """A stage count that is not a multiple of the four decode warpgroups: a
-    stage's previous half-unit went to another warpgroup (and possibly the
-    other chain), so a wait can pass on the wrong phase. Some schedule must
-    fail."""
+    """A stage count that is not a multiple of the decode warpgroups: a
+    stage's previous half-unit went to another warpgroup, so a wait can pass
+    on the wrong phase. Some schedule must fail."""
     rng = random.Random(7)
     failures = 0
     for order in cta_orders(7, 400):
         for _ in range(5):
             try:
-                run_tc(order, 6, 2, rng, 2)
+                run_tc(order, 6, 2, rng, 2, WG=4)
             except AssertionError:
                 failures += 1
     assert failures > 0

@@ -11,6 +11,7 @@ parity a wait tests can never stand for two phases at once. An earlier stage
 assignment without it (an odd stage count, groups chosen by range index) was
 safe only while copies landed in issue order."""
 
+import math
 import random
 
 import pytest
@@ -101,12 +102,18 @@ def mma_stages(bits, ukt, budget=196 * KIB):
     return min(fit, 12) & ~1
 
 
-def tc_stages(bits, slots, budget=227 * KIB):
-    """Stage count and decode warpgroups of the tcgen05 kernel's class."""
-    wg = 4
+def tc_stages(bits, slots, halves=2, budget=227 * KIB):
+    """Stage count, decode warpgroups and half-units per copy of the tcgen05
+    kernel's class: five warpgroups up to 32 row slots, four beyond; the
+    stage count a multiple of the warpgroups, and of the half-units of a
+    unit where that still leaves 8 stages or more (then one copy per unit)."""
+    wg = 5 if slots <= 32 else 4
     stage = 256 * bits * 8 + slots * 16 * 8 * 2
-    fit = (budget - 8192 - 2048) // stage
-    return (min(fit, 16) // wg) * wg, wg
+    cap = min((budget - 8192 - 2048) // stage, 16)
+    step = wg * halves // math.gcd(wg, halves)
+    if cap // step * step >= 8:
+        return cap // step * step, wg, halves
+    return cap // wg * wg, wg, 1
 
 
 def ranges(units, ctas):
@@ -164,21 +171,21 @@ def test_stage_counts_keep_each_stage_with_one_consumer(bits):
         s = mma_stages(bits, ukt)
         assert s >= 4 and s % 2 == 0, (bits, ukt, s)       # two groups, two stages each at least
     for slots in (16, 32, 64, 128):
-        s, wg = tc_stages(bits, slots)
-        assert s >= wg and s % wg == 0, (bits, slots, s)
-        # Half-unit q is decoded by warpgroup q % wg from stage q % s, so the
-        # stage's previous half-unit q - s went to the same warpgroup, and
-        # (two half-units a unit, units alternating between the chains) to
-        # the same chain.
-        for q in range(s, 4 * s):
-            assert (q - s) % wg == q % wg
-            assert ((q - s) // 2) % 2 == (q // 2) % 2 and (q - s) % 2 == q % 2
+        for halves in (1, 2):
+            s, wg, cg = tc_stages(bits, slots, halves)
+            assert s >= wg and s % wg == 0 and s % cg == 0, (bits, slots, s)
+            # Half-unit q is decoded by warpgroup q % wg from stage q % s, so
+            # the stage's previous half-unit q - s went to the same
+            # warpgroup; a copy group's half-units are consecutive.
+            for q in range(s, 4 * s):
+                assert (q - s) % wg == q % wg
+                assert (q - s) // cg % (s // cg) == q // cg % (s // cg)
 
 
 def test_stage_counts_of_the_measured_classes():
     """The counts the measurements were taken with (4 bits)."""
     assert mma_stages(4, 16) == 6
-    assert tc_stages(4, 16) == (16, 4)
-    assert tc_stages(4, 32) == (12, 4)
-    assert tc_stages(4, 64) == (8, 4)
-    assert tc_stages(4, 128) == (4, 4)
+    assert tc_stages(4, 16) == (10, 5, 2)
+    assert tc_stages(4, 32) == (10, 5, 2)
+    assert tc_stages(4, 64) == (8, 4, 2)
+    assert tc_stages(4, 128) == (4, 4, 1)

@@ -27,11 +27,15 @@
 //               Memory, added, written to this CTA's partial-sum slot, then
 //               (when the CTA owns the block, or arrives last) the output
 //               rotation, svh and the stores
-//   warps 4-19  decode: four warpgroups take half-units (8 k-tiles) in turn,
-//               half-unit q going to warpgroup q mod 4, so that a warpgroup
-//               only decodes units of one chain; thread n decodes output n's
-//               16 weights of each k-tile into Tensor Memory lane n (the MMA's
-//               A operand), in its warpgroup's A buffer
+//   decode      five warpgroups (20 warps) up to 32 row slots, four (16
+//               warps) beyond: they take half-units (8 k-tiles) in turn,
+//               half-unit q going to warpgroup q mod kWG; thread n decodes
+//               output n's 16 weights of each k-tile into Tensor Memory lane
+//               n (the MMA's A operand), in its warpgroup's A buffer, whose
+//               uses go to whichever chain each half-unit belongs to. Five
+//               warps per SM sub-partition leave fewer idle issue slots while
+//               one of them waits (LM head 4 bits, strips: 122.8 -> 120.8 us
+//               at 1 row; 6 bits 146.4 -> 143.3)
 //   next warp   weights producer: one thread copies each half-unit's packed
 //               weights into the stage ring as soon as the decode of the
 //               stage's previous half-unit is done
@@ -85,37 +89,34 @@ struct TcCfg {
   static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // SLOTS rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
-  // Four decode warpgroups: half-unit q goes to warpgroup q mod 4, so a
-  // warpgroup only ever decodes units of one chain (units at even or at odd
-  // processing positions), and the chain's MMA warp is the only reader of
-  // its A buffer.
-  static constexpr int kWG = 4;
+  // Decode warpgroups: half-unit q goes to warpgroup q mod kWG. Five (20
+  // decode warps, five per SM sub-partition) where the stages and Tensor
+  // Memory allow, four otherwise.
+  static constexpr int kWG = SLOTS <= 32 ? 5 : 4;
   // A multiple of the warpgroups, so that a stage's previous half-unit went
-  // to the same decode warpgroup (and the same chain).
-  static constexpr int kStages = (kStagesFit < 16 ? kStagesFit : 16) / kWG * kWG;
-  static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
+  // to the same decode warpgroup; and of the half-units of a copy group.
   // The stages hold half-units, but the copies and their barriers go by
   // groups of CG half-units (contiguous in both rings): a whole unit where
   // the ring is deep enough, so that each producer issues one copy a unit;
   // single half-units at 128 row slots, whose ring holds only four.
-  static constexpr int CG = kStages >= 8 ? H : 1;
+  static constexpr int kStagesCap = kStagesFit < 16 ? kStagesFit : 16;
+  static constexpr int kUnitStep = kWG * H / (kWG % H == 0 ? H : 1);  // lcm(kWG, H) for H in {1, 2}
+  static constexpr bool kWholeUnits = kStagesCap / kUnitStep * kUnitStep >= 8;
+  static constexpr int kStages = kWholeUnits ? kStagesCap / kUnitStep * kUnitStep : kStagesCap / kWG * kWG;
+  static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
+  static constexpr int CG = kWholeUnits ? H : 1;
   static constexpr int kUnitSlots = kStages / CG;
   static constexpr int kWRingOff = 0;                          // [kStages][kWBytes]
   static constexpr int kXRingOff = kStages * kWBytes;          // [kStages][kXrBytes], 1024-byte aligned
   // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
   // in kAccBufs sets that alternate between segments (so that the MMAs of a
-  // segment can start while the epilogue reads the previous one), then
-  // kABufs A buffers of 64 columns (8 k-tiles) per chain, taken in turn by
-  // the chain's half-units. With two, each of the chain's two decode
-  // warpgroups (which alternate on its half-units) has one buffer of its own;
-  // a third per chain (where the columns allow) measured no faster (LM head
-  // 4 bits, 1-16 rows: 126.9 against 124.8 us).
+  // segment can start while the epilogue reads the previous one), then one
+  // A buffer of 64 columns (8 k-tiles) per decode warpgroup.
   static constexpr int kAccBufs = SLOTS <= 64 ? 2 : 1;
-  static constexpr int kABufs = 2;
   static constexpr int kACol0 = kAccBufs * 2 * SLOTS;
-  static_assert(kACol0 + 2 * kABufs * 64 <= kTcTmemCols, "Tensor Memory columns");
-  // Warp roles: epilogue 0-3, decode 4-19, weights producer, xr producer,
-  // and one MMA warp per chain.
+  static_assert(kACol0 + kWG * 64 <= kTcTmemCols, "Tensor Memory columns");
+  // Warp roles: epilogue 0-3, decode 4 .. 4 kWG + 3, weights producer, xr
+  // producer, and one MMA warp per chain.
   static constexpr int kProdW = 4 + 4 * kWG;
   static constexpr int kProdX = kProdW + 1;
   static constexpr int kMma = kProdX + 1;  // chain 0; chain 1 is the next warp
@@ -124,7 +125,12 @@ struct TcCfg {
   static constexpr int kBarOff = kXchOff + 8192;
   // wfull, wempty, xfull, xempty per unit slot; afull, aempty per A buffer;
   // dfull, dempty per accumulator set; drain
-  static constexpr int kNumBars = 4 * kUnitSlots + 4 * kABufs + 2 * kAccBufs + 1;
+  // afull: kAFull per warpgroup, its use j on barrier j mod kAFull. A
+  // warpgroup's uses go to both chains' MMA warps (at five warpgroups), and a
+  // parity wait needs its barrier's previous phase to have been seen by the
+  // same waiter: uses j and j + 4 always belong to the same chain.
+  static constexpr int kAFull = 4;
+  static constexpr int kNumBars = 4 * kUnitSlots + (kAFull + 1) * kWG + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
   static_assert(kBytes <= kSmemBudgetWide, "shared memory");
@@ -149,8 +155,10 @@ __device__ __forceinline__ void tc_decode_kt_regs(const ColQuads<BITS>& cq, int 
 }
 
 // k-tiles of a half-unit a decode warp decodes before it waits for its A
-// buffer (held in 8 registers each).
-constexpr int kPreKt = 2;
+// buffer (held in 8 registers each): two with four decode warpgroups, one
+// with five (whose threads have 72 registers).
+template <int WG>
+constexpr int pre_kt() { return WG == 5 ? 1 : 2; }
 
 // The pass's row slots: `rows` rounded up to 16 (the MMA's N); slots past
 // `rows` read zeros.
@@ -195,10 +203,10 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   auto xempty_bar = [&](int us) { return bar0 + 8u * (3 * SU + us); };
   const uint32_t abar0 = bar0 + 8u * (4 * SU);
   // A buffer b of chain ch; accumulator set d.
-  constexpr int NB = T::kABufs;
-  auto afull_bar = [&](int ch, int b) { return abar0 + 8u * (ch * NB + b); };
-  auto aempty_bar = [&](int ch, int b) { return abar0 + 8u * (2 * NB + ch * NB + b); };
-  const uint32_t dbar0 = abar0 + 8u * (4 * NB);
+  constexpr int kAF = T::kAFull;
+  auto afull_bar = [&](int g, int j) { return abar0 + 8u * (g * kAF + (j & (kAF - 1))); };
+  auto aempty_bar = [&](int g) { return abar0 + 8u * (kAF * kWG + g); };
+  const uint32_t dbar0 = abar0 + 8u * ((kAF + 1) * kWG);
   auto dfull_bar = [&](int d) { return dbar0 + 8u * d; };
   auto dempty_bar = [&](int d) { return dbar0 + 8u * (kAccB + d); };
   const uint32_t drain = dbar0 + 8u * (2 * kAccB);
@@ -223,11 +231,10 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       mbar_init(xfull_bar(us), 1);
       mbar_init(xempty_bar(us), CG);      // the MMAs' commit, per half-unit
     }
-    for (int ch = 0; ch < 2; ++ch)
-      for (int b = 0; b < NB; ++b) {
-        mbar_init(afull_bar(ch, b), 4);   // the decoding warpgroup's 4 warps
-        mbar_init(aempty_bar(ch, b), 1);  // the MMAs' commit
-      }
+    for (int g = 0; g < kWG; ++g) {
+      for (int j = 0; j < kAF; ++j) mbar_init(afull_bar(g, j), 4);  // the warpgroup's 4 warps
+      mbar_init(aempty_bar(g), 1);                                   // the MMAs' commit
+    }
     for (int d = 0; d < kAccB; ++d) {
       mbar_init(dfull_bar(d), 2);  // one signal per chain
       mbar_init(dempty_bar(d), 4);
@@ -320,24 +327,20 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
     const int tile = n >> 4, col = n & 15;
-    // The warpgroup's chain (processing-position parity of its half-units'
-    // units) and its half-units' chain-local indices t0, t0 + 2, t0 + 4, ...
-    const int ch = H == 2 ? (wg >> 1) : (wg & 1);
-    const int t0 = H == 2 ? (wg & 1) : (wg >> 1);
+    // The warpgroup's A buffer takes its half-units wg, wg + kWG, ... in turn.
+    const uint32_t a_addr = tmem + lane_off + T::kACol0 + wg * 64;
     int s = wg;
     uint32_t sphase = 0;
     for (int j = 0;; ++j) {
       const int q = kWG * j + wg;
       if (q >= n_half) break;
-      const int t = 2 * j + t0;  // chain-local index of half-unit q
-      const int ab = t % NB;     // its A buffer; the buffer's previous user was t - NB
       bool ok = mbar_wait(wfull_bar(s / CG), sphase, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.st below is warp-collective
       const uint32_t* ws = reinterpret_cast<const uint32_t*>(smem + T::kWRingOff + s * T::kWBytes);
-      const uint32_t a_addr = tmem + lane_off + T::kACol0 + (ch * NB + ab) * 64;
       // The first kPreKt k-tiles are decoded into registers before the A
       // buffer is known to be free (the MMAs of the warpgroup's previous
       // half-unit may still be reading it), then stored once it is.
+      constexpr int kPreKt = pre_kt<kWG>();
       uint32_t pre[kPreKt][8];
       if constexpr (LAYOUT == kLayoutTiles) {
 #pragma unroll
@@ -351,14 +354,14 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       if constexpr (LAYOUT == kLayoutStrips) {
         load_col_quads<BITS>(reinterpret_cast<const uint4*>(ws + tile * 32 * BITS), col, cq0);
         tc_decode_kt_regs<BITS, 0>(cq0, col, pre[0]);
-        tc_decode_kt_regs<BITS, 1>(cq0, col, pre[1]);
+        if constexpr (kPreKt > 1) tc_decode_kt_regs<BITS, 1>(cq0, col, pre[kPreKt - 1]);
       }
-      // The A buffer: its previous half-unit's MMAs must be done.
-      // (Safe as a parity wait: this warpgroup decoded t - 2, for which it
-      // waited for the MMAs of t - 2 - NB; a chain's MMAs complete in order,
-      // so those of t - 2 NB are done, and the barrier is at most one phase
-      // behind the one waited for.)
-      if (t >= NB) ok = mbar_wait(aempty_bar(ch, ab), ((t / NB) - 1) & 1, abort_flag);
+      // The A buffer: the MMAs of the warpgroup's previous half-unit must be
+      // done. (Safe as a parity wait: the warpgroup waited for the MMAs of
+      // its half-unit before that one before it stored that one, and the
+      // MMAs of this one cannot start before the arrival below, so the
+      // barrier is exactly one phase behind or done.)
+      if (j >= 1) ok = mbar_wait(aempty_bar(wg), (j - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
 #pragma unroll
@@ -373,6 +376,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
           tmem_st8(a_addr + kt * 8, a);
         }
       } else {
+        if constexpr (kPreKt < 2) tc_decode_kt<BITS, 1>(cq0, col, a_addr + 1 * 8);
         tc_decode_kt<BITS, 2>(cq0, col, a_addr + 2 * 8);
         tc_decode_kt<BITS, 3>(cq0, col, a_addr + 3 * 8);
         ColQuads<BITS> cq;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(wempty_bar(s / CG));  // the weights of this stage have been read
-        mbar_arrive(afull_bar(ch, ab));
+        mbar_arrive(afull_bar(wg, j));
       }
       s += kWG;
       if (s >= S) {
@@ -439,15 +443,16 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
           const int q = k * H + h;
           const int s = q % S;
           const int t = (k >> 1) * H + h;  // chain-local index
-          const int ab = t % NB;
+          const int g = q % kWG;  // the warpgroup that decoded it: its use q / kWG of its A buffer
           bool ok = mbar_wait(xfull_bar(s / CG), (q / S) & 1, abort_flag);
-          ok = ok && mbar_wait(afull_bar(ch, ab), (t / NB) & 1, abort_flag);
+          const int jg = q / kWG;
+          ok = ok && mbar_wait(afull_bar(g, jg), (jg / kAF) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, ok)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = tmem + T::kACol0 + (ch * NB + ab) * 64;
+          const uint32_t a_addr = tmem + T::kACol0 + g * 64;
           const uint64_t bd0 = bdesc0 + (s / CG) * unit_step + (s % CG) * 2 * box_step;
           const uint64_t bd1 = bd0 + box_step;
           const bool first = k == kf && h == 0;  // overwrites the accumulator
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
             mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
             mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
             mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
-            mma_commit(aempty_bar(ch, ab));
+            mma_commit(aempty_bar(g));
             mma_commit(xempty_bar(s / CG));
           }
           __syncwarp();
@@ -507,11 +512,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       if (SLOTS == 16 && !shared) {
         // A block this CTA owns, in a pass of up to 16 rows: the two chains'
         // sum stays in registers, and only the pass's rows are rotated.
-        float g0[16], g1[16], v[16];
-        tmem_ld16(tmem + lane_off + (dset * 2) * SLOTS, g0);
+        float v[16], g1[16];
+        tmem_ld16(tmem + lane_off + (dset * 2) * SLOTS, v);
         tmem_ld16(tmem + lane_off + (dset * 2 + 1) * SLOTS, g1);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] = __fadd_rn(has0 ? g0[r] : 0.0f, has1 ? g1[r] : 0.0f);
+        for (int r = 0; r < 16; ++r) v[r] = __fadd_rn(has0 ? v[r] : 0.0f, has1 ? g1[r] : 0.0f);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dempty_bar(dset));  // the MMA warp may reuse the set
