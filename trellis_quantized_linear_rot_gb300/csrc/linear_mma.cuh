@@ -1,6 +1,10 @@
-// The trellis linear for decode rows on GB300: a persistent kernel with a
-// TMA-fed shared-memory pipeline; the weights are decoded straight into
-// tensor-core operand registers and multiplied with mma.sync.m16n8k16.
+// The trellis linear for decode rows on GB300, the mma.sync form: a
+// persistent kernel with a TMA-fed shared-memory pipeline; the weights are
+// decoded straight into tensor-core operand registers and multiplied with
+// mma.sync.m16n8k16. It runs the no-allocation entry point's passes of up to
+// 16 rows, whose scratch has room for its 2 x 16 x 128 partial sums per CTA
+// but not for the tcgen05 kernel's (linear_tc.cuh), which runs every other
+// pass. Both kernels give every row the same bits.
 //
 // Method: "hip exl3: the input rotation and trellis linear for decode rows",
 // section "What this changes" (second bullet): the trellis linear at 2..8 bits
@@ -8,14 +12,11 @@
 // order (so a row's bits do not depend on the rows sharing its launch), no
 // bias; the output rotation and svh finish each 128-output block.
 //
-// Why mma.sync and not tcgen05: the contraction per 16 x 16 weight tile has at
-// most 16 columns (the rows of a pass). tcgen05.mma (M = 128, N = 16) measured
-// 45-56 cycles per instruction from its single issuing thread, about 110 when
-// that thread shares its SM sub-partition with decode warps, and needs the
-// decoded weights staged through Tensor Memory; mma.sync.m16n8k16 measured 2.2
-// cycles per instruction per SM, takes the A operand straight from the decode
-// registers and is issued by every compute warp, so the contraction spreads
-// over all four sub-partitions and never stalls the decode.
+// mma.sync.m16n8k16 (2.2 cycles per instruction per SM) takes the A operand
+// straight from the decode registers and is issued by every compute warp, so
+// the contraction spreads over all four sub-partitions; the tcgen05 kernel
+// stages the decoded weights through Tensor Memory instead and is faster at
+// every row count measured (LM head 4 bits: 120.5 against 137 us at 1 row).
 //
 // Work: the (output block b, 128-input unit) grid, block-major, is cut into
 // one contiguous range per CTA (one CTA per SM). Consecutive units of one block
