@@ -7,8 +7,9 @@ simulated mbarriers with the kernel's parities. An mbarrier completes a phase
 when its expected arrivals and transaction bytes are in; a parity wait passes
 while the barrier's current phase has the other parity, which is how
 `mbarrier.try_wait.parity` behaves. Copies land in any order; tensor-core work
-(the tcgen05 kernel's MMAs and their commits) completes in issue order at
-random later times. Every buffer carries a tag naming the unit, half-unit or
+(the tcgen05 kernel's MMAs and their commits) completes at random later
+times, in issue order for each issuing warp and in any order between the
+two. Every buffer carries a tag naming the unit, half-unit or
 segment whose data it holds, and every read and every asynchronous MMA checks
 the tag: a wait that passed on a stale phase, a stage refilled while still
 being read, or an accumulator reused too early fails the test. A schedule that
@@ -59,7 +60,7 @@ class Sim:
         self.rng = rng
         self.roles = []          # [generator, pending wait or None]
         self.copies = []         # copies in flight: callables, land in any order
-        self.tensor = []         # tensor-core queue: callables, complete in order
+        self.tensor = [[], []]   # per issuing warp: callables, each queue completes in order
 
     def add(self, gen):
         self.roles.append([gen, None])
@@ -67,7 +68,8 @@ class Sim:
     def run(self, max_steps=2_000_000):
         for _ in range(max_steps):
             ready = [r for r in self.roles if r[1] is None or r[1][0].passes(r[1][1])]
-            events = len(self.copies) + (1 if self.tensor else 0)
+            queues = [t for t in self.tensor if t]
+            events = len(self.copies) + len(queues)
             if not ready and not events:
                 if self.roles:
                     names = [r[1][0].name for r in self.roles if r[1] is not None]
@@ -83,7 +85,7 @@ class Sim:
             elif pick - len(ready) < len(self.copies):
                 self.copies.pop(pick - len(ready))()
             else:
-                self.tensor.pop(0)()
+                queues[pick - len(ready) - len(self.copies)].pop(0)()
         raise AssertionError("schedule did not finish")
 
 
@@ -193,8 +195,8 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
                             ch, sg, acc[d][ch])
                         aempty[g].arrive()                   # the two commits after the MMAs
                         xempty[s // CG].arrive()
-                    sim.tensor.append(execute)
-            sim.tensor.append(dfull[d].arrive)               # commit at the segment's end
+                    sim.tensor[ch].append(execute)
+            sim.tensor[ch].append(dfull[d].arrive)           # commit at the segment's end
 
     def epilogue():
         for sg, P, L in segments():
