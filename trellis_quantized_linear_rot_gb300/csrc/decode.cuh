@@ -106,6 +106,67 @@ __device__ __forceinline__ void decode_col16_b4(uint32_t a, uint32_t b, uint32_t
   for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
 }
 
+// 2 bits: a tile is 16 words; output column n's windows start at stream bit
+// 32n - 14, i.e. at bit 18 of word a = (n - 1) mod 16, and run through word
+// b = n; window j covers bits [18 + 2j, 34 + 2j) of a:b. The windows fall
+// into four classes by their start modulo 8 bits; each class is cut out of
+// one or two helper words that align it on a byte, seven helpers serving
+// all sixteen (the generic cut takes two shifts per window).
+__device__ __forceinline__ void decode_col16_b2(uint32_t a, uint32_t b, uint32_t (&out)[8]) {
+  const uint32_t x2 = __funnelshift_l(b, a, 18);  // stream bits 18..49 (of a:b)
+  const uint32_t x4 = __funnelshift_l(b, a, 20);  // 20..51
+  const uint32_t x6 = __funnelshift_l(b, a, 22);  // 22..53
+  const uint32_t m = __funnelshift_l(b, a, 16);   // 16..47
+  const uint32_t y2 = b << 2;                     // 34..63, then zeros
+  const uint32_t y4 = b << 4;                     // 36..63
+  const uint32_t y6 = b << 6;                     // 38..63
+  const uint32_t st[16] = {hi16(x2),  hi16(x4),  hi16(x6),  mid16(m),  mid16(x2), mid16(x4), mid16(x6), hi16(b),
+                           lo16(x2),  lo16(x4),  lo16(x6),  mid16(b),  mid16(y2), mid16(y4), mid16(y6), lo16(b)};
+  uint32_t h[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) h[j] = mul1_half_plus_1024(st[j]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
+}
+
+// The 16-bit window that starts at bit P (0..31, counted from the top) of
+// word `hi` and runs on into word `lo` when P > 16: one instruction where it
+// sits on a byte boundary inside `hi`, two otherwise.
+template <int P>
+__device__ __forceinline__ uint32_t window16(uint32_t hi, uint32_t lo) {
+  static_assert(P >= 0 && P < 32, "window start");
+  if constexpr (P == 0) return hi16(hi);
+  else if constexpr (P == 8) return mid16(hi);
+  else if constexpr (P == 16) return lo16(hi);
+  else if constexpr (P < 16) return (hi >> (16 - P)) & 0xFFFFu;
+  else if constexpr (P == 24) return mid16(__funnelshift_l(lo, hi, 16));
+  else return __funnelshift_l(lo, hi, P) >> 16;
+}
+
+// 6 bits: a tile is 48 words; output column n's windows start at stream bit
+// 96n - 10, i.e. at bit 22 of word a = (3n - 1) mod 48, and run through
+// words b, c, d = 3n .. 3n+2; window j covers bits [22 + 6j, 38 + 6j) of
+// a:b:c:d. Windows 3, 7 and 15 sit on byte boundaries inside a word (one
+// instruction each), the others take two.
+template <int J>
+__device__ __forceinline__ uint32_t window_b6(const uint32_t (&w)[4]) {
+  constexpr int kStart = 22 + 6 * J;
+  constexpr int kWord = kStart / 32;
+  return window16<kStart % 32>(w[kWord], w[kWord < 3 ? kWord + 1 : 3]);
+}
+
+__device__ __forceinline__ void decode_col16_b6(const uint32_t (&w)[4], uint32_t (&out)[8]) {
+  const uint32_t st[16] = {window_b6<0>(w),  window_b6<1>(w),  window_b6<2>(w),  window_b6<3>(w),
+                           window_b6<4>(w),  window_b6<5>(w),  window_b6<6>(w),  window_b6<7>(w),
+                           window_b6<8>(w),  window_b6<9>(w),  window_b6<10>(w), window_b6<11>(w),
+                           window_b6<12>(w), window_b6<13>(w), window_b6<14>(w), window_b6<15>(w)};
+  uint32_t h[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) h[j] = mul1_half_plus_1024(st[j]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) out[k] = mul1_pair(h[2 * k], h[2 * k + 1]);
+}
+
 // 8 bits: a tile is 64 words; output column n's windows start at stream bit
 // 128n - 8, i.e. at bit 24 of word a = (4n - 1) mod 64, and run through words
 // b..e = 4n .. 4n+3; window j covers bits [24 + 8j, 40 + 8j) of a:b:c:d:e, so
@@ -131,17 +192,25 @@ __device__ __forceinline__ void decode_col16_b8(uint32_t a, uint32_t b, uint32_t
 // several k-tiles before it needs any of them.
 template <int BITS>
 struct ColWords {
-  static constexpr int kCount = BITS == 4 ? 3 : (BITS == 8 ? 5 : RowSpan<BITS>::kWords);
+  static constexpr int kCount =
+      BITS == 2 ? 2 : (BITS == 4 ? 3 : (BITS == 6 ? 4 : (BITS == 8 ? 5 : RowSpan<BITS>::kWords)));
   uint32_t w[kCount];
 };
 
 template <int BITS>
 __device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWords<BITS>& cw) {
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 2) {
+    cw.w[0] = tw[(n + 15) & 15];
+    cw.w[1] = tw[n];
+  } else if constexpr (BITS == 4) {
     cw.w[0] = tw[(2 * n + 31) & 31];
     const uint2 bc = *reinterpret_cast<const uint2*>(tw + 2 * n);
     cw.w[1] = bc.x;
     cw.w[2] = bc.y;
+  } else if constexpr (BITS == 6) {
+    cw.w[0] = tw[n == 0 ? 47 : 3 * n - 1];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) cw.w[1 + j] = tw[3 * n + j];
   } else if constexpr (BITS == 8) {
     cw.w[0] = tw[(4 * n + 63) & 63];
     const uint4 be = *reinterpret_cast<const uint4*>(tw + 4 * n);
@@ -163,8 +232,12 @@ __device__ __forceinline__ void load_col_words(const uint32_t* tw, int n, ColWor
 
 template <int BITS>
 __device__ __forceinline__ void decode_col_words(const ColWords<BITS>& cw, int n, uint32_t (&out)[8]) {
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 2) {
+    decode_col16_b2(cw.w[0], cw.w[1], out);
+  } else if constexpr (BITS == 4) {
     decode_col16_b4(cw.w[0], cw.w[1], cw.w[2], out);
+  } else if constexpr (BITS == 6) {
+    decode_col16_b6(cw.w, out);
   } else if constexpr (BITS == 8) {
     decode_col16_b8(cw.w[0], cw.w[1], cw.w[2], cw.w[3], cw.w[4], out);
   } else {
@@ -264,10 +337,17 @@ struct ColQuads {
 
 template <int BITS>
 __device__ __forceinline__ void load_col_quads(const uint4* tq, int n, ColQuads<BITS>& cq) {
-  if constexpr (BITS == 4) {
+  if constexpr (BITS == 2) {
+    cq.q[0] = tq[(n + 15) & 15];  // word n - 1 (mod 16)
+    cq.q[1] = tq[n];              // word n
+  } else if constexpr (BITS == 4) {
     cq.q[0] = tq[16 + ((n + 15) & 15)];  // word 2n - 1 (mod 32)
     cq.q[1] = tq[n];                     // word 2n
     cq.q[2] = tq[16 + n];                // word 2n + 1
+  } else if constexpr (BITS == 6) {
+    cq.q[0] = tq[n == 0 ? 47 : 3 * n - 1];  // word 3n - 1 (mod 48)
+#pragma unroll
+    for (int j = 0; j < 3; ++j) cq.q[1 + j] = tq[3 * n + j];
   } else if constexpr (BITS == 8) {
     cq.q[0] = tq[48 + ((n + 15) & 15)];  // word 4n - 1 (mod 64)
 #pragma unroll

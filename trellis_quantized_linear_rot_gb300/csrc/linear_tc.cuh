@@ -262,16 +262,18 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     // ---------------------------------------------------- weights producer
     // One copy per group of CG half-units (contiguous stages). The weights
     // are not written by the kernel before this one, so their copies start
-    // at once.
-    if (lane == 0) {
-      UnitCursor cur(order);
-      RingPos<SU> rp;
-      int h0 = 0;  // first half-unit of the group within its unit
-      int issued = 0;
-      const int n_groups = n_half / CG;
-      for (int u = 0; u < n_groups; ++u) {
-        if (u >= SU && !mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
-        const uint32_t st = smem_u32(smem + T::kWRingOff + rp.s * CG * T::kWBytes);
+    // at once. The whole warp runs the loop and one elected lane issues the
+    // copies, so that their operands are warp-uniform (a loop run by one
+    // lane issued several times as many instructions).
+    UnitCursor cur(order);
+    RingPos<SU> rp;
+    int h0 = 0;  // first half-unit of the group within its unit
+    int issued = 0;
+    const int n_groups = n_half / CG;
+    for (int u = 0; u < n_groups; ++u) {
+      if (u >= SU && !__all_sync(0xffffffffu, mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag))) break;
+      const uint32_t st = smem_u32(smem + T::kWRingOff + rp.s * CG * T::kWBytes);
+      if (elect_one()) {
         mbar_arrive_expect_tx(wfull_bar(rp.s), CG * T::kWBytes);
         if (LAYOUT == kLayoutTiles)
           tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT + h0 * kTcHalfKt,
@@ -279,51 +281,53 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
         else
           bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h0 * T::kWBytes,
                        CG * T::kWBytes, wfull_bar(rp.s));
-        issued = u + 1;
-        rp.next();
-        h0 += CG;
-        if (h0 == H) {
-          h0 = 0;
-          cur.next();
-        }
       }
-      // Let every copy this thread started land before the CTA can exit.
-      for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
-        volatile int never = 0;
-        mbar_wait(wfull_bar(u % SU), (u / SU) & 1, &never);
+      __syncwarp();
+      issued = u + 1;
+      rp.next();
+      h0 += CG;
+      if (h0 == H) {
+        h0 = 0;
+        cur.next();
       }
+    }
+    // Let every copy this warp started land before the CTA can exit.
+    for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
+      volatile int never = 0;
+      mbar_wait(wfull_bar(u % SU), (u / SU) & 1, &never);
     }
   } else if (warp == T::kProdX) {
     // --------------------------------------------------------- xr producer
     // One copy per group of CG half-units: their 2 CG chunks of 64 inputs.
-    if (lane == 0) {
-      pdl_wait_prerequisites();  // xr is written by the kernel before this one
-      UnitCursor cur(order);
-      RingPos<SU> rp;
-      int h0 = 0;
-      int issued = 0;
-      const int n_groups = n_half / CG;
-      for (int u = 0; u < n_groups; ++u) {
-        if (u >= SU && !mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag)) break;
-        const uint32_t st = smem_u32(smem + T::kXRingOff + rp.s * CG * T::kXrBytes);
+    pdl_wait_prerequisites();  // xr is written by the kernel before this one
+    UnitCursor cur(order);
+    RingPos<SU> rp;
+    int h0 = 0;
+    int issued = 0;
+    const int n_groups = n_half / CG;
+    for (int u = 0; u < n_groups; ++u) {
+      if (u >= SU && !__all_sync(0xffffffffu, mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag))) break;
+      const uint32_t st = smem_u32(smem + T::kXRingOff + rp.s * CG * T::kXrBytes);
+      if (elect_one()) {
         mbar_arrive_expect_tx(xfull_bar(rp.s), 2 * CG * xr_box_bytes);
         tma_load_3d(st, &xmap, 0, 0, cur.ub() * (UKT / 4) + h0 * 2, xfull_bar(rp.s));
-        issued = u + 1;
-        rp.next();
-        h0 += CG;
-        if (h0 == H) {
-          h0 = 0;
-          cur.next();
-        }
       }
-      for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
-        volatile int never = 0;
-        mbar_wait(xfull_bar(u % SU), (u / SU) & 1, &never);
+      __syncwarp();
+      issued = u + 1;
+      rp.next();
+      h0 += CG;
+      if (h0 == H) {
+        h0 = 0;
+        cur.next();
       }
+    }
+    for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
+      volatile int never = 0;
+      mbar_wait(xfull_bar(u % SU), (u / SU) & 1, &never);
     }
   } else if (warp >= 4 && warp < T::kProdW) {
     // -------------------------------------------------------------- decode
-    const int wg = (warp - 4) >> 2;              // takes half-units wg, wg + 4, ...
+    const int wg = (warp - 4) >> 2;              // takes half-units wg, wg + kWG, ...
     const int n = ((warp - 4) & 3) * 32 + lane;  // output of the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(((warp - 4) & 3) * 32) << 16;
     const int tile = n >> 4, col = n & 15;
@@ -457,16 +461,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
           const uint64_t bd1 = bd0 + box_step;
           const bool first = k == kf && h == 0;  // overwrites the accumulator
           if (elect_one()) {
-            mma_f16_tmemA(d_addr, a_addr, bd0, idesc, first ? 0u : 1u);
-            mma_f16_tmemA(d_addr, a_addr + 8, bd0 + 2, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 16, bd0 + 4, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 24, bd0 + 6, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 32, bd1, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 40, bd1 + 2, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 48, bd1 + 4, idesc, 1u);
-            mma_f16_tmemA(d_addr, a_addr + 56, bd1 + 6, idesc, 1u);
-            mma_commit(aempty_bar(g));
-            mma_commit(xempty_bar(s / CG));
+            // the A buffer and the xr slice are free once these complete
+            mma8_commit2(d_addr, a_addr, bd0, bd1, idesc, first ? 0u : 1u, aempty_bar(g), xempty_bar(s / CG));
           }
           __syncwarp();
         }
@@ -504,9 +500,14 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       const bool ok = mbar_wait_sleepy(dfull_bar(dset), (sg / kAccB) & 1, abort_flag, 64);
       if (!group_all(1, 128, ok)) break;  // the named barriers below need all 128 threads
       tc_fence_after();
-      const int c_first = cta_of_unit(static_cast<long long>(b) * order.UB, p.units, p.ctas);
-      const int c_last = cta_of_unit(static_cast<long long>(b + 1) * order.UB - 1, p.units, p.ctas);
-      const bool shared = c_first != c_last;
+      // Shared with other CTAs unless this CTA's range holds the whole block
+      // (the CTAs that share it are found only then: 64-bit divisions).
+      const bool shared = seg_hi - seg_lo != order.UB;
+      int c_first = c, c_last = c;
+      if (shared) {
+        c_first = cta_of_unit(static_cast<long long>(b) * order.UB, p.units, p.ctas);
+        c_last = cta_of_unit(static_cast<long long>(b + 1) * order.UB - 1, p.units, p.ctas);
+      }
       const int slot = shared ? partial_slot(c, b, p) : 2;
       float* mine = p.partials + (static_cast<size_t>(c) * kTcPartialSlots + slot) * slot_floats;
       if (SLOTS == 16 && !shared) {

@@ -195,14 +195,33 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo
   return d;
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
+// A half-unit's 8 MMAs into D[tmem] (K = 16 each; A columns a, a + 8, ...,
+// a + 56; B descriptors d0, d0 + 2, d0 + 4, d0 + 6 for k-tiles 0-3 and d1 ..
+// d1 + 6 for 4-7, advanced in 16-byte units inside the swizzle atom), the
+// first one overwriting D unless `accumulate`, then a commit to each of two
+// barriers. One block, so that the operands of the eight steps are formed
+// once: issued by one thread.
+__device__ __forceinline__ void mma8_commit2(uint32_t d_tmem, uint32_t a, uint64_t d0, uint64_t d1, uint32_t idesc,
+                                             uint32_t accumulate, uint32_t bar_a, uint32_t bar_b) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 e1, e2, e3, f1, f2, f3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.eq.b32 q, 0, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t"
+      "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"
+      "add.u64 e1, %2, 2;\n\tadd.u64 e2, %2, 4;\n\tadd.u64 e3, %2, 6;\n\t"
+      "add.u64 f1, %3, 2;\n\tadd.u64 f2, %3, 4;\n\tadd.u64 f3, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], e1, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], e2, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], e3, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], %3, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], f1, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], f2, %4, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], f3, %4, q;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+      ::"r"(d_tmem), "r"(a), "l"(d0), "l"(d1), "r"(idesc), "r"(accumulate), "r"(bar_a), "r"(bar_b)
       : "memory");
 }
 
