@@ -36,10 +36,10 @@
 //               warps per SM sub-partition leave fewer idle issue slots while
 //               one of them waits (LM head 4 bits, strips: 122.8 -> 120.8 us
 //               at 1 row; 6 bits 146.4 -> 143.3)
-//   next warp   weights producer: one thread copies each half-unit's packed
-//               weights into the stage ring as soon as the decode of the
-//               stage's previous half-unit is done
-//   next warp   xr producer: one thread copies each half-unit's xr slice
+//   next warp   weights producer: one elected lane copies each half-unit's
+//               packed weights into the stage ring as soon as the decode of
+//               the stage's previous half-unit is done
+//   next warp   xr producer: one elected lane copies each half-unit's xr slice
 //               (one tensor copy of two chunks of 64 inputs x the pass's row
 //               slots, with the 128-byte swizzle: the MMA's K-major B layout)
 //               as soon as the MMAs of the stage's previous half-unit are done
@@ -53,11 +53,14 @@
 // A stage holds a half-unit's weights and its xr slice, each part with its
 // own full and empty barriers: the weights are read by the decode and the
 // xr slice by the MMAs, so each part is refilled as soon as its reader is
-// done, by its own thread. A single thread issuing every copy was the
+// done, by its own warp. A single thread issuing every copy was the
 // kernel's bottleneck (measured on the GB300: a thread issuing 1-D bulk
 // copies alone manages one copy per ~500 cycles whatever its size, most of it
 // the thread's own chain of dependent instructions), so the two producers
-// keep their loops short and work from counters, not divisions.
+// keep their loops short and work from counters, not divisions. Each runs
+// its loop on the whole warp, like the MMA warps, so that the copies'
+// operands are warp-uniform: the same loop on lane 0 alone issued more
+// instructions, which the decode warps of its sub-partition paid for.
 //
 // Ordering with the kernels around this one (programmatic dependent launch):
 // every thread that reads memory the kernel before may write (xr, by the xr
