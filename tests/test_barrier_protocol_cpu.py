@@ -106,13 +106,17 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
     go to whichever chain the half-unit belongs to, signalled through four
     full barriers (use j on barrier j mod 4); one MMA warp per chain (units
     at even / odd processing positions), each issuing its chain's MMAs in
-    order; ACC accumulator sets alternating between segments.
+    order, a whole unit's at once (after waiting for all its half-units)
+    where one copy brings the unit; ACC accumulator sets alternating between
+    segments.
     `plant` names a fault to plant: "w_early" refills a stage's weights
     without waiting for the decode, "x_early" its xr slice without waiting
     for the MMAs, "no_dempty" starts a segment without waiting for the
     readout of its accumulator set, "a_early" decodes into an A buffer
     without waiting for the MMAs that read it before, "one_afull" signals
-    every use of an A buffer on a single full barrier."""
+    every use of an A buffer on a single full barrier, "two_units" has an
+    MMA warp wait for two of its chain's units before issuing either (a
+    warpgroup's next half-unit then waits on MMAs that wait on it)."""
     sim = Sim(rng)
     n_half = order.n_units * H
     CG = H if (S >= 8 and S % (WG * H // (H if WG % H == 0 else 1)) == 0) else 1
@@ -176,17 +180,28 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
             if kf >= P + L:
                 dfull[d].arrive()                            # no unit of this chain here
                 continue
-            for k in range(kf, P + L, 2):
-                for h in range(H):
-                    q = k * H + h
+            # The chain's half-units in groups: every wait of a group first,
+            # then its MMAs (a whole unit where one copy brings it). The
+            # "two_units" plant groups a unit with the chain's next one.
+            ks = list(range(kf, P + L, 2))
+            if plant == "two_units":
+                groups = [[k * H + h for k in ks[i:i + 2] for h in range(H)] for i in range(0, len(ks), 2)]
+            else:
+                B = H if CG == H else 1
+                groups = [[k * H + h0 + i for i in range(B)] for k in ks for h0 in range(0, H, B)]
+            for grp in groups:
+                for q in grp:
+                    s = q % S
+                    assert ((q // H) & 1) == ch
+                    if s % CG == 0:                          # the first half-unit of its copy
+                        yield wait(xfull[s // CG], (q // S) & 1)
+                    jj = q // WG
+                    yield wait(afull[q % WG][jj % AF], (jj // AF) & 1)
+                for q in grp:
                     s = q % S
                     g = q % WG
-                    assert ((q // H) & 1) == ch
-                    yield wait(xfull[s // CG], (q // S) & 1)
-                    jj = q // WG
-                    yield wait(afull[g][jj % AF], (jj // AF) & 1)
 
-                    def execute(q=q, s=s, g=g, sg=sg, d=d, first=(k == kf and h == 0)):
+                    def execute(q=q, s=s, g=g, sg=sg, d=d, first=(q == kf * H)):
                         assert xtag[s] == q, "MMA of %d found stage %d's xr of %s" % (q, s, xtag[s])
                         assert abuf[g] == q, "MMA of %d found A buffer %d holding %s" % (q, g, abuf[g])
                         if first:
@@ -314,7 +329,7 @@ def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, WG):
             run_tc(order, S, H, rng, ACC, WG=WG)
 
 
-@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early", "one_afull"])
+@pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early", "one_afull", "two_units"])
 def test_tc_planted_faults_are_caught(plant):
     """A producer that refills its part of a stage without waiting for that
     part's reader, or a chain that starts a segment in an accumulator set

@@ -444,28 +444,42 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
         continue;
       }
       const uint32_t d_addr = tmem + (dset * 2 + ch) * SLOTS;
+      // The segment's half-units in groups of B: the MMA warp waits for a
+      // whole group, then issues it at once (B = H where one copy brings the
+      // whole unit, so one xr wait a unit). Fewer loop passes mean fewer
+      // instructions on this warp's sub-partition, which its decode warps pay
+      // for. A group never spans two half-units of one warpgroup (B <= 2 <
+      // kWG), so no decode waits on MMAs that wait on it.
+      constexpr int B = CG == H ? H : 1;
       for (int k = kf; k < P + L && !stop; k += 2) {
 #pragma unroll 1
-        for (int h = 0; h < H; ++h) {
-          const int q = k * H + h;
-          const int s = q % S;
-          const int t = (k >> 1) * H + h;  // chain-local index
-          const int g = q % kWG;  // the warpgroup that decoded it: its use q / kWG of its A buffer
-          bool ok = mbar_wait(xfull_bar(s / CG), (q / S) & 1, abort_flag);
-          const int jg = q / kWG;
-          ok = ok && mbar_wait(afull_bar(g, jg), (jg / kAF) & 1, abort_flag);
+        for (int h0 = 0; h0 < H; h0 += B) {
+          int s[B], g[B];  // per half-unit: its stage and the warpgroup that decoded it
+          bool ok = true;
+#pragma unroll
+          for (int i = 0; i < B; ++i) {
+            const int q = k * H + h0 + i;
+            s[i] = q % S;
+            g[i] = q % kWG;
+            const int jg = q / kWG;  // its use of that warpgroup's A buffer
+            if (i == 0) ok = ok && mbar_wait(xfull_bar(s[i] / CG), (q / S) & 1, abort_flag);
+            ok = ok && mbar_wait(afull_bar(g[i], jg), (jg / kAF) & 1, abort_flag);
+          }
           if (!__all_sync(0xffffffffu, ok)) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = tmem + T::kACol0 + g * 64;
-          const uint64_t bd0 = bdesc0 + (s / CG) * unit_step + (s % CG) * 2 * box_step;
-          const uint64_t bd1 = bd0 + box_step;
-          const bool first = k == kf && h == 0;  // overwrites the accumulator
           if (elect_one()) {
-            // the A buffer and the xr slice are free once these complete
-            mma8_commit2(d_addr, a_addr, bd0, bd1, idesc, first ? 0u : 1u, aempty_bar(g), xempty_bar(s / CG));
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+              const uint32_t a_addr = tmem + T::kACol0 + g[i] * 64;
+              const uint64_t bd0 = bdesc0 + (s[i] / CG) * unit_step + (s[i] % CG) * 2 * box_step;
+              const bool first = k == kf && h0 + i == 0;  // overwrites the accumulator
+              // the A buffer and the xr slice are free once these complete
+              mma8_commit2(d_addr, a_addr, bd0, bd0 + box_step, idesc, first ? 0u : 1u, aempty_bar(g[i]),
+                           xempty_bar(s[i] / CG));
+            }
           }
           __syncwarp();
         }
