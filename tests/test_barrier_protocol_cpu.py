@@ -97,7 +97,7 @@ def wait(bar, parity):
 # --------------------------------------------------------------------------
 # The tcgen05 kernel: producer, WG decode warpgroups, MMA warp, epilogue.
 
-def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
+def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4, SW=None):
     """The tcgen05 kernel: a weights producer and an xr producer, each
     refilling its part of a unit's stages (one copy per unit of H half-units
     where the ring allows) once that part's readers are done (the decode
@@ -121,8 +121,10 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
     n_half = order.n_units * H
     CG = H if (S >= 8 and S % (WG * H // (H if WG % H == 0 else 1)) == 0) else 1
     SU = S // CG             # copy slots: the barriers go by copies
-    wfull = [Bar("wfull%d" % s, 1) for s in range(SU)]
-    wempty = [Bar("wempty%d" % s, 4 * CG) for s in range(SU)]
+    SW = S if SW is None else SW   # the weights ring may be deeper than the xr ring
+    SUW = SW // CG
+    wfull = [Bar("wfull%d" % s, 1) for s in range(SUW)]
+    wempty = [Bar("wempty%d" % s, 4 * CG) for s in range(SUW)]
     xfull = [Bar("xfull%d" % s, 1) for s in range(SU)]
     xempty = [Bar("xempty%d" % s, CG) for s in range(SU)]
     AF = 1 if plant == "one_afull" else 4  # full barriers per warpgroup: use j on barrier j % AF
@@ -130,12 +132,12 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
     aempty = [Bar("aempty%d" % g, 1) for g in range(WG)]
     dfull = [Bar("dfull%d" % d, 2) for d in range(ACC)]
     dempty = [Bar("dempty%d" % d, 4) for d in range(ACC)]
-    wtag = [None] * S        # half-unit whose weights a stage holds
+    wtag = [None] * SW       # half-unit whose weights a stage holds
     xtag = [None] * S        # half-unit whose xr slice a stage holds
     abuf = [None] * WG  # half-unit whose decoded weights a warpgroup's A buffer holds
     acc = [[None, None] for _ in range(ACC)]  # segment whose sums a chain's accumulator holds
 
-    def producer(full, empty, tag, wait_empty):
+    def producer(full, empty, tag, wait_empty, SU):
         for u in range(n_half // CG):
             us = u % SU
             if u >= SU and wait_empty:
@@ -152,8 +154,8 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
         j = 0
         while WG * j + wg < n_half:
             q = WG * j + wg
-            s = q % S
-            yield wait(wfull[s // CG], (q // S) & 1)
+            s = q % SW
+            yield wait(wfull[s // CG], (q // SW) & 1)
             if j >= 1 and plant != "a_early":
                 yield wait(aempty[wg], (j - 1) & 1)
             assert wtag[s] == q, "decode of %d read stage %d holding %s" % (q, s, wtag[s])
@@ -228,15 +230,15 @@ def run_tc(order, S, H, rng, ACC=2, plant=None, WG=4):
             for _ in range(4):
                 dempty[d].arrive()
 
-    sim.add(producer(wfull, wempty, wtag, plant != "w_early"))
-    sim.add(producer(xfull, xempty, xtag, plant != "x_early"))
+    sim.add(producer(wfull, wempty, wtag, plant != "w_early", SUW))
+    sim.add(producer(xfull, xempty, xtag, plant != "x_early", SU))
     for wg in range(WG):
         sim.add(decode(wg))
     sim.add(mma(0))
     sim.add(mma(1))
     sim.add(epilogue())
     sim.run()
-    assert all(wtag[s] is not None for s in range(min(S, n_half)))
+    assert all(wtag[s] is not None for s in range(min(SW, n_half)))
 
 
 # --------------------------------------------------------------------------
@@ -317,16 +319,21 @@ def cta_orders(seed, n):
         yield SegmentOrder(u0, u1, ub)
 
 
-# (stages, half-units per unit, accumulator sets, decode warpgroups): the
-# kernel's row-slot classes (five warpgroups up to 32 row slots: 10 stages,
-# or 15 at one half-unit per unit; four beyond: 8 and 4 stages) and others.
-@pytest.mark.parametrize("S,H,ACC,WG", [(10, 2, 2, 5), (15, 1, 2, 5), (8, 2, 2, 4), (4, 2, 1, 4), (16, 2, 2, 4),
-                                        (12, 2, 2, 4), (8, 1, 2, 4), (4, 1, 1, 4), (20, 2, 2, 5)])
-def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, WG):
-    rng = random.Random(100 * S + 10 * H + ACC + 1000 * WG)
-    for order in cta_orders(S * 4 + H + WG, 60):
+# (xr stages, half-units per unit, accumulator sets, decode warpgroups,
+# weights stages): every row-slot class the kernel is built for (2..8 bits;
+# 16, 32, 64, 128 row slots; one or two half-units per unit), then others.
+REAL_CLASSES = [(10, 2, 2, 5, 10), (8, 2, 2, 4, 8), (4, 2, 1, 4, 4), (15, 1, 2, 5, 15), (8, 1, 2, 4, 8),
+                (4, 1, 1, 4, 20), (4, 1, 1, 4, 12), (10, 1, 2, 5, 10), (4, 1, 1, 4, 8), (4, 1, 2, 4, 12),
+                (4, 1, 1, 4, 4), (6, 1, 2, 5, 10), (4, 1, 2, 4, 8)]
+
+
+@pytest.mark.parametrize("S,H,ACC,WG,SW", REAL_CLASSES + [(16, 2, 2, 4, 16), (12, 2, 2, 4, 12), (20, 2, 2, 5, 20),
+                                                         (10, 2, 2, 5, 20)])
+def test_tc_kernel_protocol_under_random_schedules(S, H, ACC, WG, SW):
+    rng = random.Random(100 * S + 10 * H + ACC + 1000 * WG + 7 * SW)
+    for order in cta_orders(S * 4 + H + WG + SW, 60):
         for _ in range(3):
-            run_tc(order, S, H, rng, ACC, WG=WG)
+            run_tc(order, S, H, rng, ACC, WG=WG, SW=SW)
 
 
 @pytest.mark.parametrize("plant", ["w_early", "x_early", "no_dempty", "a_early", "one_afull", "two_units"])
@@ -365,6 +372,24 @@ def test_planted_fault_is_caught():
                 run_tc(order, 6, 2, rng, 2, WG=4)
             except AssertionError:
                 failures += 1
+    assert failures > 0
+
+
+def test_odd_xr_ring_below_two_stages_per_warpgroup_is_caught():
+    """Control for the xr ring rule: five xr slots of single half-units with
+    five warpgroups (what the 8-bit, 32-row-slot class had) let the MMA warp
+    of half-unit q + 5 test the slot's barrier before the other chain's copy
+    of q landed. Some schedule must fail."""
+    failures = 0
+    for seed in range(40):
+        rng = random.Random(seed)
+        for order in cta_orders(seed + 1000, 60):
+            try:
+                run_tc(order, 5, 1, rng, 2, WG=5, SW=10)
+            except AssertionError:
+                failures += 1
+        if failures:
+            break
     assert failures > 0
 
 

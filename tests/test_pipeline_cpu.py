@@ -116,6 +116,22 @@ def tc_stages(bits, slots, halves=2, budget=227 * KIB):
     return cap // wg * wg, wg, 1
 
 
+def tc_rings(bits, slots, halves=2, budget=227 * KIB):
+    """The tcgen05 kernel's two rings: (xr stages, weights stages, decode
+    warpgroups, half-units per copy). The xr ring is the base stage count,
+    but never an odd number of copy slots below two stages per warpgroup;
+    where the base leaves fewer than two stages per warpgroup and copies
+    bring whole units, the weights ring takes the rest of shared memory, a
+    multiple of its step, capped at 24."""
+    s, wg, cg = tc_stages(bits, slots, halves, budget)
+    wbytes, xbytes = 256 * bits * 8, slots * 16 * 8 * 2
+    sx = s + cg if (s < 2 * wg and (s // cg) % 2) else s
+    step = wg * halves // math.gcd(wg, halves) if cg == halves else wg
+    wcap = min((budget - 8192 - 2048 - sx * xbytes) // wbytes, 24)
+    sw = wcap // step * step if (s < 2 * wg and cg == halves and wcap // step * step > s) else s
+    return sx, sw, wg, cg
+
+
 def ranges(units, ctas):
     return [(c * units // ctas, (c + 1) * units // ctas) for c in range(ctas)]
 
@@ -189,3 +205,23 @@ def test_stage_counts_of_the_measured_classes():
     assert tc_stages(4, 32) == (10, 5, 2)
     assert tc_stages(4, 64) == (8, 4, 2)
     assert tc_stages(4, 128) == (4, 4, 1)
+
+
+def test_ring_depths_keep_their_waits_within_one_phase():
+    for bits in (2, 3, 4, 5, 6, 8):
+        for halves in ((2, 1) if bits <= 5 else (1,)):
+            for slots in (16, 32, 64, 128):
+                sx, sw, wg, cg = tc_rings(bits, slots, halves)
+                assert sw % wg == 0 and sw % cg == 0 and sx % cg == 0, (bits, slots, halves)
+                # below two stages per warpgroup the xr slots come in even numbers,
+                # so that a slot's consecutive uses go to one chain
+                assert sx >= 2 * wg or (sx // cg) % 2 == 0, (bits, slots, halves)
+                assert sw * 256 * bits * 8 + sx * slots * 16 * 8 * 2 + 8192 + 2048 <= 227 * KIB
+
+
+def test_ring_depths_of_the_measured_classes():
+    assert tc_rings(4, 16) == (10, 10, 5, 2)
+    assert tc_rings(8, 32, 1) == (6, 10, 5, 1)
+    assert tc_rings(6, 64, 1) == (4, 12, 4, 1)
+    assert tc_rings(8, 64, 1) == (4, 8, 4, 1)
+    assert tc_rings(4, 128) == (4, 4, 4, 1)

@@ -108,9 +108,30 @@ struct TcCfg {
   static constexpr int kStages = kWholeUnits ? kStagesCap / kUnitStep * kUnitStep : kStagesCap / kWG * kWG;
   static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
   static constexpr int CG = kWholeUnits ? H : 1;
-  static constexpr int kUnitSlots = kStages / CG;
-  static constexpr int kWRingOff = 0;                          // [kStages][kWBytes]
-  static constexpr int kXRingOff = kStages * kWBytes;          // [kStages][kXrBytes], 1024-byte aligned
+  // The xr ring: kStages, but never an odd number of copy slots below two
+  // stages per decode warpgroup. Consecutive uses of an xr slot then belong
+  // to one chain, i.e. one MMA warp, wherever nothing else orders them: with
+  // five slots of single half-units (8 bits, 32 row slots) the MMA warp of
+  // half-unit q + 5 could test the slot's barrier before the copy of q (the
+  // other chain's) had landed, and a parity wait cannot tell those phases
+  // apart. The host simulation of every row-slot class found that schedule.
+  static constexpr int kXStages = (kStages < 2 * kWG && (kStages / CG) % 2 != 0) ? kStages + CG : kStages;
+  static constexpr int kUnitSlots = kXStages / CG;  // xr copy slots
+  // The weights ring may be deeper than the xr ring: where the wide xr
+  // slices leave fewer than two stages per decode warpgroup (6 and 8 bits at
+  // 32 and 64 row slots), the weights take the rest of shared memory, a
+  // multiple of the warpgroups (and of the copy group) again. Measured on
+  // the GB300, LM head: 6 bits, 64 rows 164.8 -> 157.9 us; 8 bits, 32 rows
+  // 148.3 -> 132.0 us, 64 rows 166.9 -> 159.7 us. Where the ring already held
+  // two stages per warpgroup, a deeper one gained nothing.
+  static constexpr int kWStep = kWholeUnits ? kUnitStep : kWG;
+  static constexpr int kWFit = (kSmemBudgetWide - 8192 - 2048 - kXStages * kXrBytes) / kWBytes;
+  static constexpr int kWCap = kWFit < 24 ? kWFit : 24;
+  static constexpr bool kDeepW = kStages < 2 * kWG && CG == H && kWCap / kWStep * kWStep > kStages;
+  static constexpr int kWStages = kDeepW ? kWCap / kWStep * kWStep : kStages;
+  static constexpr int kWUnitSlots = kWStages / CG;
+  static constexpr int kWRingOff = 0;                          // [kWStages][kWBytes]
+  static constexpr int kXRingOff = kWStages * kWBytes;         // [kXStages][kXrBytes], 1024-byte aligned
   // Tensor Memory: the accumulators of the two chains (SLOTS columns each),
   // in kAccBufs sets that alternate between segments (so that the MMAs of a
   // segment can start while the epilogue reads the previous one), then one
@@ -124,7 +145,7 @@ struct TcCfg {
   static constexpr int kProdX = kProdW + 1;
   static constexpr int kMma = kProdX + 1;  // chain 0; chain 1 is the next warp
   static constexpr int kThreads = (kMma + 2) * 32;
-  static constexpr int kXchOff = kStages * kStageBytes;
+  static constexpr int kXchOff = kXRingOff + kXStages * kXrBytes;
   static constexpr int kBarOff = kXchOff + 8192;
   // wfull, wempty, xfull, xempty per unit slot; afull, aempty per A buffer;
   // dfull, dempty per accumulator set; drain
@@ -133,7 +154,7 @@ struct TcCfg {
   // parity wait needs its barrier's previous phase to have been seen by the
   // same waiter: uses j and j + 4 always belong to the same chain.
   static constexpr int kAFull = 4;
-  static constexpr int kNumBars = 4 * kUnitSlots + (kAFull + 1) * kWG + 2 * kAccBufs + 1;
+  static constexpr int kNumBars = 2 * kWUnitSlots + 2 * kUnitSlots + (kAFull + 1) * kWG + 2 * kAccBufs + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 64;
   static_assert(kBytes <= kSmemBudgetWide, "shared memory");
@@ -187,12 +208,15 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
                              const __grid_constant__ CUtensorMap xmap, const MmaParams p) {
   constexpr int H = UKT / kTcHalfKt;  // half-units per unit
   using T = TcCfg<BITS, SLOTS, H>;
-  constexpr int S = T::kStages;
+  constexpr int S = T::kXStages;     // xr stages
   constexpr int CG = T::CG;           // half-units per copy
-  constexpr int SU = T::kUnitSlots;   // copy slots
+  constexpr int SU = T::kUnitSlots;   // xr copy slots
+  constexpr int SW = T::kWStages;     // weights stages
+  constexpr int SUW = T::kWUnitSlots;  // weights copy slots
   constexpr int kWG = T::kWG;
   constexpr int kAccB = T::kAccBufs;
-  static_assert(S >= kWG && S % kWG == 0, "stages must stay with one decode warpgroup");
+  static_assert(SW >= kWG && SW % kWG == 0 && SW % CG == 0, "weights stages must stay with one decode warpgroup");
+  static_assert(S % CG == 0, "xr stages");
   extern __shared__ __align__(1024) uint8_t smem[];
   float(*xch)[128] = reinterpret_cast<float(*)[128]>(smem + T::kXchOff);
   const uint32_t bar0 = smem_u32(smem + T::kBarOff);
@@ -201,10 +225,10 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + T::kMiscOff + 8);
   // Barriers of copy slot us (holding half-unit stages us * CG .. + CG - 1).
   auto wfull_bar = [&](int us) { return bar0 + 8u * us; };
-  auto wempty_bar = [&](int us) { return bar0 + 8u * (SU + us); };
-  auto xfull_bar = [&](int us) { return bar0 + 8u * (2 * SU + us); };
-  auto xempty_bar = [&](int us) { return bar0 + 8u * (3 * SU + us); };
-  const uint32_t abar0 = bar0 + 8u * (4 * SU);
+  auto wempty_bar = [&](int us) { return bar0 + 8u * (SUW + us); };
+  auto xfull_bar = [&](int us) { return bar0 + 8u * (2 * SUW + us); };
+  auto xempty_bar = [&](int us) { return bar0 + 8u * (2 * SUW + SU + us); };
+  const uint32_t abar0 = bar0 + 8u * (2 * SUW + 2 * SU);
   // A buffer b of chain ch; accumulator set d.
   constexpr int kAF = T::kAFull;
   auto afull_bar = [&](int g, int j) { return abar0 + 8u * (g * kAF + (j & (kAF - 1))); };
@@ -228,9 +252,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     // are multiples of 1024).
     *abort_flag = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
     *last_flag = 0;
-    for (int us = 0; us < SU; ++us) {
+    for (int us = 0; us < SUW; ++us) {
       mbar_init(wfull_bar(us), 1);
       mbar_init(wempty_bar(us), 4 * CG);  // the 4 warps of each half-unit's decoding warpgroup
+    }
+    for (int us = 0; us < SU; ++us) {
       mbar_init(xfull_bar(us), 1);
       mbar_init(xempty_bar(us), CG);      // the MMAs' commit, per half-unit
     }
@@ -269,12 +295,12 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     // copies, so that their operands are warp-uniform (a loop run by one
     // lane issued several times as many instructions).
     UnitCursor cur(order);
-    RingPos<SU> rp;
+    RingPos<SUW> rp;
     int h0 = 0;  // first half-unit of the group within its unit
     int issued = 0;
     const int n_groups = n_half / CG;
     for (int u = 0; u < n_groups; ++u) {
-      if (u >= SU && !__all_sync(0xffffffffu, mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag))) break;
+      if (u >= SUW && !__all_sync(0xffffffffu, mbar_wait(wempty_bar(rp.s), rp.phase ^ 1u, abort_flag))) break;
       const uint32_t st = smem_u32(smem + T::kWRingOff + rp.s * CG * T::kWBytes);
       if (elect_one()) {
         mbar_arrive_expect_tx(wfull_bar(rp.s), CG * T::kWBytes);
@@ -295,9 +321,9 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
       }
     }
     // Let every copy this warp started land before the CTA can exit.
-    for (int u = issued - SU > 0 ? issued - SU : 0; u < issued; ++u) {
+    for (int u = issued - SUW > 0 ? issued - SUW : 0; u < issued; ++u) {
       volatile int never = 0;
-      mbar_wait(wfull_bar(u % SU), (u / SU) & 1, &never);
+      mbar_wait(wfull_bar(u % SUW), (u / SUW) & 1, &never);
     }
   } else if (warp == T::kProdX) {
     // --------------------------------------------------------- xr producer
@@ -401,8 +427,8 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
         mbar_arrive(afull_bar(wg, j));
       }
       s += kWG;
-      if (s >= S) {
-        s -= S;
+      if (s >= SW) {
+        s -= SW;
         sphase ^= 1u;
       }
     }
