@@ -352,7 +352,7 @@ def test_tc_planted_faults_are_caught(plant):
     assert failures > 0
 
 
-@pytest.mark.parametrize("S", [4, 6, 8, 12])
+@pytest.mark.parametrize("S", [4, 6, 8, 10, 12])
 def test_mma_kernel_protocol_under_random_schedules(S):
     rng = random.Random(S)
     for order in cta_orders(50 + S, 80):
