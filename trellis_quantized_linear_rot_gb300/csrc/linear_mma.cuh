@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto dfull_bar = [&](int d) { return bar0 + 8u * (2 * S + d); };
   auto dempty_bar = [&](int d) { return bar0 + 8u * (2 * S + 2 + d); };
 
-  const int warp = threadIdx.x >> 5;
+  // The warp index through a shuffle from lane 0, so that the compiler knows
+  // it is the same in every lane (role values in uniform registers).
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   constexpr int kProducerWarp = 4 + kComputeWarps;
   const int c = blockIdx.x;

@@ -238,7 +238,11 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   auto dempty_bar = [&](int d) { return dbar0 + 8u * (kAccB + d); };
   const uint32_t drain = dbar0 + 8u * (2 * kAccB);
 
-  const int warp = threadIdx.x >> 5;
+  // The warp index through a shuffle from lane 0: the compiler then knows it
+  // is the same in every lane, so the roles' loop values live in uniform
+  // registers (measured on the GB300: 115.0 -> 111.2 M instructions a launch,
+  // 72 -> 70 registers with no spills; LM head 4 bits 118.7 -> 115.6 us).
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x;
   const SegmentOrder order(range_start(c, p.units, p.ctas), range_start(c + 1, p.units, p.ctas),
