@@ -321,10 +321,12 @@ def cta_orders(seed, n):
 
 # (xr stages, half-units per unit, accumulator sets, decode warpgroups,
 # weights stages): every row-slot class the kernel is built for (2..8 bits;
-# 16, 32, 64, 128 row slots; one or two half-units per unit), then others.
-REAL_CLASSES = [(10, 2, 2, 5, 10), (8, 2, 2, 4, 8), (4, 2, 1, 4, 4), (15, 1, 2, 5, 15), (8, 1, 2, 4, 8),
-                (4, 1, 1, 4, 20), (4, 1, 1, 4, 12), (10, 1, 2, 5, 10), (4, 1, 1, 4, 8), (4, 1, 2, 4, 12),
-                (4, 1, 1, 4, 4), (6, 1, 2, 5, 10), (4, 1, 2, 4, 8)]
+# 16, 32, 64, 128 row slots; one or two half-units per unit; the list
+# `tc_rings` of the pipeline test derives), then others.
+REAL_CLASSES = [(4, 1, 1, 4, 4), (4, 1, 1, 4, 8), (4, 1, 1, 4, 12), (4, 1, 1, 4, 20), (4, 1, 2, 4, 8),
+                (4, 1, 2, 4, 12), (4, 2, 1, 4, 4), (6, 1, 2, 5, 10), (6, 1, 2, 6, 12), (8, 1, 2, 4, 8),
+                (8, 2, 2, 4, 8), (10, 1, 2, 5, 10), (10, 2, 2, 5, 10), (12, 1, 2, 6, 12), (12, 2, 2, 6, 12),
+                (15, 1, 2, 5, 15)]
 
 
 @pytest.mark.parametrize("S,H,ACC,WG,SW", REAL_CLASSES + [(16, 2, 2, 4, 16), (12, 2, 2, 4, 12), (20, 2, 2, 5, 20),

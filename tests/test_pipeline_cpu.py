@@ -104,10 +104,11 @@ def mma_stages(bits, ukt, budget=196 * KIB):
 
 def tc_stages(bits, slots, halves=2, budget=227 * KIB):
     """Stage count, decode warpgroups and half-units per copy of the tcgen05
-    kernel's class: five warpgroups up to 32 row slots, four beyond; the
-    stage count a multiple of the warpgroups, and of the half-units of a
-    unit where that still leaves 8 stages or more (then one copy per unit)."""
-    wg = 5 if slots <= 32 else 4
+    kernel's class: six warpgroups at 16 row slots and 4, 6 or 8 bits, five
+    otherwise up to 32 row slots, four beyond; the stage count a multiple of
+    the warpgroups, and of the half-units of a unit where that still leaves
+    8 stages or more (then one copy per unit)."""
+    wg = 6 if (slots == 16 and bits in (4, 6, 8)) else (5 if slots <= 32 else 4)
     stage = 256 * bits * 8 + slots * 16 * 8 * 2
     cap = min((budget - 8192 - 2048) // stage, 16)
     step = wg * halves // math.gcd(wg, halves)
@@ -201,7 +202,8 @@ def test_stage_counts_keep_each_stage_with_one_consumer(bits):
 def test_stage_counts_of_the_measured_classes():
     """The counts the measurements were taken with (4 bits)."""
     assert mma_stages(4, 16) == 6
-    assert tc_stages(4, 16) == (10, 5, 2)
+    assert tc_stages(4, 16) == (12, 6, 2)
+    assert tc_stages(2, 16) == (10, 5, 2)
     assert tc_stages(4, 32) == (10, 5, 2)
     assert tc_stages(4, 64) == (8, 4, 2)
     assert tc_stages(4, 128) == (4, 4, 1)
@@ -220,7 +222,8 @@ def test_ring_depths_keep_their_waits_within_one_phase():
 
 
 def test_ring_depths_of_the_measured_classes():
-    assert tc_rings(4, 16) == (10, 10, 5, 2)
+    assert tc_rings(4, 16) == (12, 12, 6, 2)
+    assert tc_rings(8, 16, 1) == (6, 12, 6, 1)
     assert tc_rings(8, 32, 1) == (6, 10, 5, 1)
     assert tc_rings(6, 64, 1) == (4, 12, 4, 1)
     assert tc_rings(8, 64, 1) == (4, 8, 4, 1)

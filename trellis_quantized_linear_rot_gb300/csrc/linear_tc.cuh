@@ -27,15 +27,17 @@
 //               Memory, added, written to this CTA's partial-sum slot, then
 //               (when the CTA owns the block, or arrives last) the output
 //               rotation, svh and the stores
-//   decode      five warpgroups (20 warps) up to 32 row slots, four (16
-//               warps) beyond: they take half-units (8 k-tiles) in turn,
+//   decode      six warpgroups (24 warps) in the 16-row-slot class at 4, 6
+//               and 8 bits, five (20 warps) otherwise up to 32 row slots,
+//               four (16 warps) beyond: they take half-units (8 k-tiles) in turn,
 //               half-unit q going to warpgroup q mod kWG; thread n decodes
 //               output n's 16 weights of each k-tile into Tensor Memory lane
 //               n (the MMA's A operand), in its warpgroup's A buffer, whose
-//               uses go to whichever chain each half-unit belongs to. Five
-//               warps per SM sub-partition leave fewer idle issue slots while
-//               one of them waits (LM head 4 bits, strips: 122.8 -> 120.8 us
-//               at 1 row; 6 bits 146.4 -> 143.3)
+//               uses go to whichever chain each half-unit belongs to. More
+//               decode warps per SM sub-partition leave fewer idle issue
+//               slots while one of them waits (LM head 4 bits, strips, four
+//               to five: 122.8 -> 120.8 us at 1 row; k-tile order, five to
+//               six: 115.6 -> 114.6)
 //   next warp   weights producer: one elected lane copies each half-unit's
 //               packed weights into the stage ring as soon as the decode of
 //               the stage's previous half-unit is done
@@ -92,10 +94,14 @@ struct TcCfg {
   static constexpr int kXrBytes = SLOTS * 16 * kTcHalfKt * 2;  // SLOTS rows x 128 inputs, fp16
   static constexpr int kStageBytes = kWBytes + kXrBytes;
   static constexpr int kStagesFit = (kSmemBudgetWide - 8192 - 2048) / kStageBytes;
-  // Decode warpgroups: half-unit q goes to warpgroup q mod kWG. Five (20
-  // decode warps, five per SM sub-partition) where the stages and Tensor
-  // Memory allow, four otherwise.
-  static constexpr int kWG = SLOTS <= 32 ? 5 : 4;
+  // Decode warpgroups: half-unit q goes to warpgroup q mod kWG. Six (24
+  // decode warps, six per SM sub-partition, 64 registers a thread) in the
+  // 16-row-slot class at 4, 6 and 8 bits, five up to 32 row slots otherwise,
+  // four beyond. Measured on the GB300 (LM head, 1 / 8 / 16 rows): 4 bits
+  // 115.6 / 117.5 / 118.1 -> 114.6 / 114.7 / 116.7 us; 6 and 8 bits 1-2 us
+  // faster; wkv 6144 -> 25,600 level. At 2, 3 and 5 bits, and at 32 row
+  // slots, six were level or slower (wkv 5 bits 42.9 -> 44.9 us).
+  static constexpr int kWG = (SLOTS == 16 && (BITS == 4 || BITS == 6 || BITS == 8)) ? 6 : (SLOTS <= 32 ? 5 : 4);
   // A multiple of the warpgroups, so that a stage's previous half-unit went
   // to the same decode warpgroup; and of the half-units of a copy group.
   // The stages hold half-units, but the copies and their barriers go by
@@ -150,7 +156,7 @@ struct TcCfg {
   // wfull, wempty, xfull, xempty per unit slot; afull, aempty per A buffer;
   // dfull, dempty per accumulator set; drain
   // afull: kAFull per warpgroup, its use j on barrier j mod kAFull. A
-  // warpgroup's uses go to both chains' MMA warps (at five warpgroups), and a
+  // warpgroup's uses go to both chains' MMA warps (at five and six), and a
   // parity wait needs its barrier's previous phase to have been seen by the
   // same waiter: uses j and j + 4 always belong to the same chain.
   static constexpr int kAFull = 4;
@@ -180,9 +186,9 @@ __device__ __forceinline__ void tc_decode_kt_regs(const ColQuads<BITS>& cq, int 
 
 // k-tiles of a half-unit a decode warp decodes before it waits for its A
 // buffer (held in 8 registers each): two with four decode warpgroups, one
-// with five (whose threads have 72 registers).
+// with five or six (whose threads have 72 or 64 registers).
 template <int WG>
-constexpr int pre_kt() { return WG == 5 ? 1 : 2; }
+constexpr int pre_kt() { return WG >= 5 ? 1 : 2; }
 
 // The pass's row slots: `rows` rounded up to 16 (the MMA's N); slots past
 // `rows` read zeros.
