@@ -426,9 +426,32 @@ def time_config(tf, dev, name, i_f, o_f, bits, rows_list, out_dtype, layout, ite
             evs.append((e0, e1))
         torch.cuda.synchronize()
         us = statistics.median(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+        # The same calls replayed from a CUDA graph (16 calls a replay): the
+        # device time of a call without the host's per-call launch cost,
+        # which bounds the eager figure of the small layers.
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.graph(g, stream=side):
+            for k in range(16):
+                lin(xr[:r], ws[k % n_copies], svh, bits, o_f, y=y)
+        torch.cuda.synchronize()
+        g.replay()
+        gevs = []
+        for k in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            g.replay()
+            e1.record(st)
+            gevs.append((e0, e1))
+        torch.cuda.synchronize()
+        gus = statistics.median(e0.elapsed_time(e1) for e0, e1 in gevs) * 1e3 / 16
+        del g
         lb = launch_bytes(r, i_f, o_f, bits, 2 if out_dtype == "fp16" else 4)
         out[str(r)] = {"us_median": us, "weight_gbs": weight_bytes(i_f, o_f, bits) * math.ceil(r / 128) / us / 1e3,
-                       "rows_per_s": r / (us * 1e-6), "hbm_frac": lb / us / 1e3 / peak}
+                       "rows_per_s": r / (us * 1e-6), "hbm_frac": lb / us / 1e3 / peak,
+                       "graph_us_per_call": gus}
     tf.tf_device_error()
     del ws
     return {"in_features": i_f, "out_features": o_f, "bits": bits, "out_dtype": out_dtype,

@@ -4,8 +4,9 @@ at every output block its work split cuts between CTAs; the contract's
 planted controls (the real kernels launched wrongly from the host must go
 red); rows past the batch left untouched; the contract's shape list at every
 width with five byte-identical runs; non-finite inputs in every input dtype;
-calls back to back on one stream and one workspace; and the codebook at
-every one of the 65,536 trellis states.
+calls back to back on one stream and one workspace; a decode step replayed
+from a CUDA graph; and the codebook at every one of the 65,536 trellis
+states.
 
 Page: "hip exl3: the input rotation and trellis linear for decode rows"
 (TensorFold pull request #3314), sections "Checks on this head" and "Kernel
@@ -224,6 +225,48 @@ def test_back_to_back_calls_on_one_stream_and_workspace():
         xr = host(xr_t)
         assert np.array_equal(bits16(xr), bits16(o.rot_in_f32(x, suh)))
         assert_close_f32(host(y_t), o.linear_f64(xr, o.decode_matrix(tr, i_f, o_f, bits), svh))
+
+
+# ------------------------------------------------- replay in a CUDA graph
+def test_rot_in_and_linear_replay_in_a_cuda_graph_bit_identical():
+    """A decode step captured once in a CUDA graph (rot_in and the linear for
+    three layers of different shapes, widths and row counts, all on the
+    library's one workspace) and replayed: every replay gives the eager
+    results bit for bit, and the eager results match the oracle. The launches
+    hold no allocation and no synchronisation once the workspace exists."""
+    cases = [(512, 128, 4, 1), (6144, 1024, 6, 4), (2048, 8192, 3, 16)]
+    prepared = []
+    for k, (i_f, o_f, bits, rows) in enumerate(cases):
+        x, suh, svh, tr = inputs(rows, i_f, o_f, bits, c=140 + k)
+        prepared.append((x, suh, svh, tr, dev(x), dev(suh), dev(svh), dev(tr)))
+    eager = []
+    for (i_f, o_f, bits, rows), p in zip(cases, prepared):
+        xr_t = tf.tf_rot_in(p[4], p[5])
+        eager.append(host(tf.tf_trellis_linear(xr_t, p[7], p[6], bits, o_f)))
+    torch.cuda.synchronize()
+    tf.tf_device_error()
+    # outputs and intermediates the graph writes into
+    xrs = [torch.empty((rows, i_f), dtype=torch.float16, device="cuda") for (i_f, o_f, bits, rows) in cases]
+    ys = [torch.empty((rows, o_f), dtype=torch.float32, device="cuda") for (i_f, o_f, bits, rows) in cases]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for (i_f, o_f, bits, rows), p, xr_t, y_t in zip(cases, prepared, xrs, ys):
+            tf.tf_rot_in(p[4], p[5], xr=xr_t)
+            tf.tf_trellis_linear(xr_t, p[7], p[6], bits, o_f, y=y_t)
+    for _ in range(3):
+        for y_t in ys:
+            y_t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        tf.tf_device_error()
+        for want, y_t in zip(eager, ys):
+            assert np.array_equal(host(y_t).view(np.uint32), want.view(np.uint32))
+    for (i_f, o_f, bits, rows), p, want in zip(cases, prepared, eager):
+        x, suh, svh, tr = p[:4]
+        xr = o.rot_in_f32(x, suh)
+        assert_close_f32(want, o.linear_f64(xr, o.decode_matrix(tr, i_f, o_f, bits), svh))
 
 
 # ------------------------------------------------- every codebook state
