@@ -46,16 +46,17 @@
 //               slots, with the 128-byte swizzle: the MMA's K-major B layout)
 //               as soon as the MMAs of the stage's previous half-unit are done
 //   last two    MMA, one warp per chain: each issues its chain's MMAs in
-//               input order (one elected lane of the whole warp); the first
+//               input order (one elected lane of the whole warp), a whole
+//               unit's 16 at once where one copy brings the unit; the first
 //               allocates Tensor Memory. One issuing thread retires about one
 //               MMA (M = 128, N = 16, K = 16) per 65 cycles, and two issuing
 //               warps twice as many (measured on the GB300), so each chain
 //               has its own warp; one issuing warp for both chains was busy
 //               most of the time and held the decode up.
-// A stage holds a half-unit's weights and its xr slice, each part with its
-// own full and empty barriers: the weights are read by the decode and the
-// xr slice by the MMAs, so each part is refilled as soon as its reader is
-// done, by its own warp. A single thread issuing every copy was the
+// A half-unit's weights and its xr slice sit in two rings, each with its
+// own depth and its own full and empty barriers: the weights are read by
+// the decode and the xr slice by the MMAs, so each part is refilled as soon
+// as its reader is done, by its own warp. A single thread issuing every copy was the
 // kernel's bottleneck (measured on the GB300: a thread issuing 1-D bulk
 // copies alone manages one copy per ~500 cycles whatever its size, most of it
 // the thread's own chain of dependent instructions), so the two producers
