@@ -377,6 +377,23 @@ def test_planted_fault_is_caught():
     assert failures > 0
 
 
+def test_xr_ring_off_the_chain_period_is_caught():
+    """Control: six xr slots of single half-units at two half-units per unit
+    (a chain period of four) with five warpgroups: a slot's consecutive uses
+    alternate chains. Some schedule must fail."""
+    failures = 0
+    for seed in range(60):
+        rng = random.Random(seed)
+        for order in cta_orders(seed + 3000, 60):
+            try:
+                run_tc(order, 6, 2, rng, 1, WG=5, SW=5)
+            except AssertionError:
+                failures += 1
+        if failures:
+            break
+    assert failures > 0
+
+
 def test_odd_xr_ring_below_two_stages_per_warpgroup_is_caught():
     """Control for the xr ring rule: five xr slots of single half-units with
     five warpgroups (what the 8-bit, 32-row-slot class had) let the MMA warp

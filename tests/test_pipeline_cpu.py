@@ -120,13 +120,14 @@ def tc_stages(bits, slots, halves=2, budget=227 * KIB):
 def tc_rings(bits, slots, halves=2, budget=227 * KIB):
     """The tcgen05 kernel's two rings: (xr stages, weights stages, decode
     warpgroups, half-units per copy). The xr ring is the base stage count,
-    but never an odd number of copy slots below two stages per warpgroup;
+    rounded up to a multiple of the chains' period (2 * halves) below two
+    stages per warpgroup;
     where the base leaves fewer than two stages per warpgroup and copies
     bring whole units, the weights ring takes the rest of shared memory, a
     multiple of its step, capped at 24."""
     s, wg, cg = tc_stages(bits, slots, halves, budget)
     wbytes, xbytes = 256 * bits * 8, slots * 16 * 8 * 2
-    sx = s + cg if (s < 2 * wg and (s // cg) % 2) else s
+    sx = (s // (2 * halves) + 1) * 2 * halves if (s < 2 * wg and s % (2 * halves)) else s
     step = wg * halves // math.gcd(wg, halves) if cg == halves else wg
     wcap = min((budget - 8192 - 2048 - sx * xbytes) // wbytes, 24)
     sw = wcap // step * step if (s < 2 * wg and cg == halves and wcap // step * step > s) else s
@@ -215,9 +216,9 @@ def test_ring_depths_keep_their_waits_within_one_phase():
             for slots in (16, 32, 64, 128):
                 sx, sw, wg, cg = tc_rings(bits, slots, halves)
                 assert sw % wg == 0 and sw % cg == 0 and sx % cg == 0, (bits, slots, halves)
-                # below two stages per warpgroup the xr slots come in even numbers,
-                # so that a slot's consecutive uses go to one chain
-                assert sx >= 2 * wg or (sx // cg) % 2 == 0, (bits, slots, halves)
+                # below two stages per warpgroup the xr ring is a multiple of the
+                # chains' period, so that a slot's consecutive uses go to one chain
+                assert sx >= 2 * wg or sx % (2 * halves) == 0, (bits, slots, halves)
                 assert sw * 256 * bits * 8 + sx * slots * 16 * 8 * 2 + 8192 + 2048 <= 227 * KIB
 
 

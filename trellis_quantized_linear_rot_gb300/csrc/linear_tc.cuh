@@ -115,14 +115,16 @@ struct TcCfg {
   static constexpr int kStages = kWholeUnits ? kStagesCap / kUnitStep * kUnitStep : kStagesCap / kWG * kWG;
   static_assert(kStages >= kWG, "one stage per decode warpgroup at least");
   static constexpr int CG = kWholeUnits ? H : 1;
-  // The xr ring: kStages, but never an odd number of copy slots below two
-  // stages per decode warpgroup. Consecutive uses of an xr slot then belong
-  // to one chain, i.e. one MMA warp, wherever nothing else orders them: with
-  // five slots of single half-units (8 bits, 32 row slots) the MMA warp of
-  // half-unit q + 5 could test the slot's barrier before the copy of q (the
-  // other chain's) had landed, and a parity wait cannot tell those phases
-  // apart. The host simulation of every row-slot class found that schedule.
-  static constexpr int kXStages = (kStages < 2 * kWG && (kStages / CG) % 2 != 0) ? kStages + CG : kStages;
+  // The xr ring: kStages, but below two stages per decode warpgroup always a
+  // multiple of the chains' period (2 H half-units), so that consecutive
+  // uses of an xr slot belong to one chain, i.e. one MMA warp, wherever
+  // nothing else orders them: with five slots of single half-units (8 bits,
+  // 32 row slots) the MMA warp of half-unit q + 5 could test the slot's
+  // barrier before the copy of q (the other chain's) had landed, and a
+  // parity wait cannot tell those phases apart. The host simulation of every
+  // row-slot class found that schedule.
+  static constexpr int kXStages =
+      (kStages < 2 * kWG && kStages % (2 * H) != 0) ? (kStages / (2 * H) + 1) * (2 * H) : kStages;
   static constexpr int kUnitSlots = kXStages / CG;  // xr copy slots
   // The weights ring may be deeper than the xr ring: where the wide xr
   // slices leave fewer than two stages per decode warpgroup (6 and 8 bits at
