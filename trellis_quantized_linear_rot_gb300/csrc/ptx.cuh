@@ -91,13 +91,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-// Shared-memory 32-bit load by shared-window address.
-__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
-  return v;
-}
-
 // Named barrier over `nthreads` threads that also returns the AND of `pred`
 // over them, so a group can leave a loop together.
 __device__ __forceinline__ bool group_all(int bar_id, int nthreads, bool pred) {
@@ -114,9 +107,6 @@ __device__ __forceinline__ bool group_all(int bar_id, int nthreads, bool pred) {
 }
 
 // ------------------------------------------------------------------ fences
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
