@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       UnitCursor cur(order);
       UnitCursor xcur(order);
+      const uint64_t wpolicy = l2_evict_first();  // weights: first out of L2
       int s = 0;
       int round = 0;
       // The first stages' weight copies need nothing from the kernel before
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < pre; ++i) {
         const uint32_t st = smem_u32(smem + i * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(i), L::kStageBytes);
-        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(i));
+        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(i), wpolicy);
         cur.next();
       }
       pdl_wait_prerequisites();
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (round > 0 && !mbar_wait_sleepy(empty_bar(s), (round - 1) & 1, abort_flag, 128)) break;
         const uint32_t st = smem_u32(smem + s * L::kStageBytes);
         mbar_arrive_expect_tx(full_bar(s), L::kStageBytes);
-        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(s));
+        tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT, full_bar(s), wpolicy);
         tma_load_3d(st + C::kWUnitBytes, &xmap, 0, 0, cur.ub() * (UKT / 4), full_bar(s));
         issued = i + 1;
         cur.next();

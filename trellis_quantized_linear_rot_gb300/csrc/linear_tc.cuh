@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     UnitCursor cur(order);
     RingPos<SUW> rp;
     int h0 = 0;  // first half-unit of the group within its unit
+    const uint64_t wpolicy = l2_evict_first();  // weights: first out of L2
     int issued = 0;
     const int n_groups = n_half / CG;
     for (int u = 0; u < n_groups; ++u) {
@@ -319,10 +320,10 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
         mbar_arrive_expect_tx(wfull_bar(rp.s), CG * T::kWBytes);
         if (LAYOUT == kLayoutTiles)
           tma_load_2d(st, &wmap, static_cast<int>(cur.bb) * 32 * BITS, cur.ub() * UKT + h0 * kTcHalfKt,
-                      wfull_bar(rp.s));
+                      wfull_bar(rp.s), wpolicy);
         else
           bulk_load_1d(st, p.strips + (cur.bb * order.UB + cur.ub()) * (256LL * BITS * UKT) + h0 * T::kWBytes,
-                       CG * T::kWBytes, wfull_bar(rp.s));
+                       CG * T::kWBytes, wfull_bar(rp.s), wpolicy);
       }
       __syncwarp();
       issued = u + 1;
