@@ -6,10 +6,12 @@ like the page's ("hip exl3: the input rotation and trellis linear for decode
 rows", section "What this changes": x ~ N(0,1) fp16, suh/svh random sign *
 U[0.5,1.5], uniformly random packed trellis bits).
 
-A step is the whole hot path for each row count: tf_rot_in then the trellis
-linear. The weights are in the k-tile-major order of the packed tiles
+A step is the whole hot path for each row count: the rotation of the rows
+and the trellis linear, by default as one call (tf_rot_in_linear: one launch
+that rotates, then sums; `--calls separate` times tf_rot_in then
+tf_trellis_linear, two launches). The weights are in the k-tile-major order of the packed tiles
 (`--layout strips` times the library's strips order instead, repacked once
-at load time, outside the timed region). The packed weights
+at load time, outside the timed region, through the two calls). The packed weights
 (331 MB each) exceed the 129 MB L2; two copies alternate between calls, so no
 call finds its weights in L2.
 
@@ -18,9 +20,9 @@ nothing recorded between the launches. The roofline is HBM: the fraction is
 the linear's algorithmic bytes per launch (packed weights + xr + svh + y)
 over its CUDA-event time, against the measured HBM copy bandwidth; those
 per-launch times come from a second timed pass of the K steps with an event
-pair around each (rot_in, linear) call. The decode's issue-slot view (lane
-operations per second against the SMs' issue peak) is reported beside it
-under "alu".
+pair around each call (the fused call, or the rot_in and linear pair). The
+decode's issue-slot view (lane operations per second against the SMs' issue
+peak) is reported beside it under "alu".
 
 Also measured in the same run, outside the headline: every other
 configuration the page's projections give (wk, wkv at 1/4/16 rows, the bit
@@ -75,11 +77,13 @@ def weight_bytes(i=IN_F, o=OUT_F, b=BITS):
     return i * o * b // 8
 
 
-def launch_bytes(rows, i=IN_F, o=OUT_F, b=BITS, out_elem=4):
+def launch_bytes(rows, i=IN_F, o=OUT_F, b=BITS, out_elem=4, fused=False):
     """Algorithmic bytes of one linear call: packed weights (streamed once per
-    pass of up to 128 rows), fp16 xr, fp16 svh, the output."""
+    pass of up to 128 rows), fp16 xr, fp16 svh, the output. The fused call
+    reads fp16 x in place of xr and also reads suh and writes xr."""
     passes = max(1, math.ceil(rows / 128))
-    return passes * weight_bytes(i, o, b) + rows * i * 2 + o * 2 + rows * o * out_elem
+    extra = (i * 2 + rows * i * 2) if fused else 0
+    return passes * weight_bytes(i, o, b) + rows * i * 2 + o * 2 + rows * o * out_elem + extra
 
 
 # Lane operations the method's decode needs per weight: window cut, 32-bit
@@ -344,11 +348,18 @@ def cpu_baseline(all_blocks=60, one_blocks=6):
                          "sample": sample_text(one_blocks, 1) + ", %.1f s wall" % secs1}}
 
 
+def fused_calls(args):
+    """Whether the step runs the fused call (the k-tile order only)."""
+    return getattr(args, "calls", "fused") == "fused" and args.layout == "tiles"
+
+
 def bench_config(args, world):
     """The workload description both arms print."""
     return {"workload": WORKLOAD, "rows": list(ROWS), "in_features": IN_F, "out_features": OUT_F,
             "bits": BITS, "out_dtype": "fp32", "weight_bytes_per_call": weight_bytes(),
             "layout": args.layout,
+            "calls": ("fused: tf_rot_in_linear, one launch per call" if fused_calls(args)
+                      else "separate: tf_rot_in then tf_trellis_linear"),
             "l2": "inputs larger than L2: 331 MB packed weights per call, two copies alternated",
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
@@ -477,6 +488,26 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
 
+    if args.only_configs:
+        # Only the named configurations, nothing else on the device: the
+        # command the per-configuration ncu captures use.
+        names = [n.strip() for n in args.only_configs.split(",")]
+        known = [c[0] for c in CONFIGS]
+        for n in names:
+            if n not in known:
+                raise SystemExit("unknown configuration %r (known: %s)" % (n, ", ".join(known)))
+        peak, _ = measured_peaks()
+        by_config = {}
+        for name, i_f, o_f, bits, rows_list, odt in CONFIGS:
+            if name in names:
+                by_config[name] = time_config(tf, dev, name, i_f, o_f, bits, rows_list, odt, args.layout,
+                                              args.config_iters, peak)
+        if rank == 0:
+            print(json.dumps({"by_config": by_config}))
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
     # Inputs (untimed): two copies of the packed weights, x for 16 rows.
     tr_np = synth.make_trellis(IN_F, OUT_F, BITS, synth.SEED_TRELLIS + 2 + BITS)
     tr0 = torch.from_numpy(tr_np.view(np.int32)).to(dev)
@@ -486,6 +517,7 @@ def run_ours(args):
     tr1 = tr0.clone()
     linear = tf.tf_trellis_linear_strips if args.layout == "strips" else tf.tf_trellis_linear
     trs = (tr0, tr1)
+    fused = fused_calls(args)
     x = torch.from_numpy(synth.make_x(max(ROWS), IN_F, synth.SEED_X + 2)).to(dev)
     suh = torch.from_numpy(synth.make_scale(IN_F, synth.SEED_SUH + 2)).to(dev)
     svh = torch.from_numpy(synth.make_scale(OUT_F, synth.SEED_SVH + 2)).to(dev)
@@ -505,10 +537,13 @@ def run_ours(args):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            tf.tf_rot_in(x[:r], suh, xr=xrs[r])
             t = trs[call[0] % 2]
             call[0] += 1
-            linear(xrs[r], t, svh, BITS, OUT_F, y=ys[r])
+            if fused:
+                tf.tf_rot_in_linear(x[:r], suh, t, svh, BITS, OUT_F, xr=xrs[r], y=ys[r])
+            else:
+                tf.tf_rot_in(x[:r], suh, xr=xrs[r])
+                linear(xrs[r], t, svh, BITS, OUT_F, y=ys[r])
             if record:
                 e1.record(stream)
                 ev[r].append((e0, e1))
@@ -561,9 +596,9 @@ def run_ours(args):
         ds = [a.elapsed_time(b) for a, b in ev[r]]
         us = statistics.median(ds) * 1e3
         per_rows[str(r)] = {"us_median": us, "weight_gbs": weight_bytes() / us / 1e3, "rows_per_s": r / (us * 1e-6),
-                            "hbm_gbs": launch_bytes(r) / us / 1e3, "hbm_frac": launch_bytes(r) / us / 1e3 / peak}
+                            "hbm_gbs": launch_bytes(r, fused=fused) / us / 1e3, "hbm_frac": launch_bytes(r, fused=fused) / us / 1e3 / peak}
         dur_sum += sum(ds)
-        byte_sum += launch_bytes(r) * len(ds)
+        byte_sum += launch_bytes(r, fused=fused) * len(ds)
         launches += len(ds)
     achieved = byte_sum / (dur_sum * 1e-3) / 1e9
     traffic = profiled_traffic()
@@ -586,8 +621,12 @@ def run_ours(args):
     def e2e_step():
         x_dev = x_host.to(dev, non_blocking=True)
         for r in ROWS:
-            xr = tf.tf_rot_in(x_dev[:r], suh)
-            y = linear(xr, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
+            if fused:
+                _, y = tf.tf_rot_in_linear(x_dev[:r], suh, trs[call[0] % 2], svh, BITS, OUT_F,
+                                           out_dtype=torch.float32)
+            else:
+                xr = tf.tf_rot_in(x_dev[:r], suh)
+                y = linear(xr, trs[call[0] % 2], svh, BITS, OUT_F, out_dtype=torch.float32)
             call[0] += 1
             done = torch.cuda.Event()
             done.record(stream)
@@ -637,8 +676,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_avg, "peak_source": peak_kind,
                      "kernel": DOMINANT_KERNEL, "kernel_hash": kernel_hash(),
-                     "timing": "CUDA events around each (rot_in, linear) pair over a second pass of the K steps",
-                     "bytes_per_launch": {str(r): launch_bytes(r) for r in ROWS},
+                     "timing": ("CUDA events around each fused (rotation + linear) call" if fused else
+                                "CUDA events around each (rot_in, linear) pair") + " over a second pass of the K steps",
+                     "bytes_per_launch": {str(r): launch_bytes(r, fused=fused) for r in ROWS},
                      "alu": {"achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
                              "frac": alu_achieved / alu_peak, "ops_per_weight": DECODE_OPS_PER_WEIGHT,
                              "peak_source": "%d SMs x 4 issue slots x 32 lanes x %.0f MHz" % (num_sms, max_sm_mhz())}},
@@ -647,7 +687,7 @@ def run_ours(args):
             "value": e2e_value, "unit": "GB/s",
             "h2d_bytes_per_step": max(ROWS) * IN_F * 2,
             "d2h_bytes_per_step": sum(r * OUT_F * 4 for r in ROWS)},
-        "gpu_launches": 2 * len(ROWS) * args.steps,
+        "gpu_launches": (1 if fused else 2) * len(ROWS) * args.steps,
         "cpu_baseline": cpu,
         "by_config": by_config,
     }
@@ -666,9 +706,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations")
     ap.add_argument("--config-iters", type=int, default=20)
+    ap.add_argument("--only-configs", default="",
+                    help="time only these configurations (comma-separated names), print their by_config "
+                         "entries and nothing else (for per-configuration profiling)")
     ap.add_argument("--load-s", type=float, default=0.5,
                     help="untimed steps run under the clock sampler before the timed region (seconds)")
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
+    ap.add_argument("--calls", choices=["fused", "separate"], default="fused",
+                    help="the step's calls: the fused rotation + linear (default) or rot_in then the linear "
+                         "(always for --layout strips)")
     ap.add_argument("--layout", choices=["tiles", "strips"], default="tiles",
                     help="weight storage order: the k-tile-major tiles (the default) or strips "
                          "(repacked once at load, untimed)")

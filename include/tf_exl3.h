@@ -112,6 +112,32 @@ tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh
                             int out_features, int bits, void* stream);
 
 /*
+ * tf_rot_in_linear -- tf_rot_in followed by tf_trellis_linear in one launch
+ * per pass ("What this changes": callers issue rot_in, then the linear, for
+ * each projection of a decode step; here the pair is one call). Arguments
+ * as in those two calls: x [rows][in_features] of dtype x_dtype, suh
+ * [in_features] fp16, xr [rows][in_features] fp16 (written: the rotated
+ * rows, the caller's memory), trellis in the k-tile-major order, svh, y,
+ * out_dtype, rows, in_features, out_features, bits. xr and y are the same
+ * bits as tf_rot_in then tf_trellis_linear give.
+ * Inside the launch, the CTAs that are running hand the pass's (row,
+ * 128-block) units out among themselves through a counter and rotate them
+ * into xr; each CTA's tensor copies of xr start once every unit is written.
+ * No CTA waits for another to be resident: one running CTA rotates every
+ * unit if it is alone. The wait is bounded like every wait in the kernels
+ * (1 s); past it the launch gives up and tf_device_error reports
+ * TF_ERR_TIMEOUT. The launch uses three counters of the library's
+ * per-device workspace (back at zero after each launch), so, like
+ * tf_trellis_linear, it must not run concurrently with another linear call
+ * on the same device.
+ * Refusals: those of tf_rot_in and tf_trellis_linear.
+ */
+tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr,
+                           const void* trellis, const void* svh, void* y, int out_dtype,
+                           int rows, int in_features, int out_features, int bits,
+                           void* stream);
+
+/*
  * tf_trellis_linear_strips -- tf_trellis_linear on the same tiles stored in
  * the "strips" order ("Checks on this head": the decode test runs on the
  * checkpoint's tile layout and on the strips layout; the page does not spell

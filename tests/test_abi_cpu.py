@@ -110,6 +110,22 @@ def test_rot_in_refusals(lib):
     assert f(NUL, tf.TF_F16, NUL, NUL, 0, 512, S) == tf.TF_OK
 
 
+def test_rot_in_linear_refusals(lib):
+    f = lib.tf_rot_in_linear
+    def call(x=P, xdt=tf.TF_F16, suh=P, xr=P, tr=P, svh=P, y=P, dt=tf.TF_F32, rows=1, i=512, o=128, bits=4):
+        return f(x, xdt, suh, xr, tr, svh, y, dt, rows, i, o, bits, S)
+    assert call(rows=-1) == tf.TF_ERR_SHAPE
+    assert call(i=500) == tf.TF_ERR_SHAPE
+    assert call(o=0) == tf.TF_ERR_SHAPE
+    assert call(bits=7) == tf.TF_ERR_BITS
+    assert call(xdt=7) == tf.TF_ERR_DTYPE
+    assert call(dt=3) == tf.TF_ERR_DTYPE
+    for k in ("x", "suh", "xr", "tr", "svh", "y"):
+        assert call(**{k: NUL}) == tf.TF_ERR_NULL, k
+        assert call(**{k: MIS}) == tf.TF_ERR_ALIGN, k
+    assert call(rows=0, x=NUL, xr=NUL, y=NUL) == tf.TF_OK
+
+
 def test_decode_refusals(lib):
     f = lib.tf_trellis_decode
     assert f(P, P, 512, 100, 4, S) == tf.TF_ERR_SHAPE

@@ -24,6 +24,7 @@ SIGNATURES = {
     "tf_abi_version": (_I, []),
     "tf_rot_in": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP]),
     "tf_trellis_linear": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tf_rot_in_linear": (_I, [_VP, _I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_strips": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_to_strips": (_I, [_VP, _VP, _I, _I, _I, _VP]),
@@ -150,6 +151,29 @@ def tf_trellis_linear(xr, trellis, svh, bits, out_features, out_dtype=None, y=No
                                  in_f, out_features, bits, _stream(stream))
     _check(st, "tf_trellis_linear")
     return y
+
+
+def tf_rot_in_linear(x, suh, trellis, svh, bits, out_features, out_dtype=None, xr=None, y=None, stream=None):
+    """tf_rot_in then tf_trellis_linear in one launch per pass (see tf_rot_in_linear).
+
+    x: [rows, in] fp16/bf16/fp32; suh: [in] fp16; trellis in the k-tile-major
+    order; svh: [out] fp16. xr (written, [rows, in] fp16) and y are allocated
+    when not given. Returns (xr, y).
+    """
+    import torch
+    rows, in_f = x.shape
+    for t, n in ((x, "x"), (suh, "suh"), (trellis, "trellis"), (svh, "svh")):
+        _contig(t, n)
+    if xr is None:
+        xr = torch.empty((rows, in_f), dtype=torch.float16, device=x.device)
+    if y is None:
+        y = torch.empty((rows, out_features), dtype=out_dtype or torch.float32, device=x.device)
+    _contig(xr, "xr")
+    _contig(y, "y")
+    st = lib().tf_rot_in_linear(_ptr(x), _dtype_code(x.dtype), _ptr(suh), _ptr(xr), _ptr(trellis), _ptr(svh),
+                                _ptr(y), _dtype_code(y.dtype), rows, in_f, out_features, bits, _stream(stream))
+    _check(st, "tf_rot_in_linear")
+    return xr, y
 
 
 def tf_trellis_linear_strips(xr, strips, svh, bits, out_features, out_dtype=None, y=None, stream=None):

@@ -72,7 +72,7 @@ tf_status ensure_workspace(DeviceCtx* c) {
   std::lock_guard<std::mutex> lock(g_ctx_mutex);
   if (c->partials != nullptr) return TF_OK;
   const size_t slots = static_cast<size_t>(c->num_sms);
-  const size_t counters = kMaxOutFeatures / 128;
+  const size_t counters = kMaxOutFeatures / 128 + 3;  // + the fused rotation's three counts
   void* part = nullptr;
   void* cnt = nullptr;
   cudaError_t e = cudaMalloc(&part, slots * kPartialFloatsPerCta * sizeof(float));
@@ -228,6 +228,57 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
     p.bits = bits;
     cudaError_t e = launch_trellis_linear_mma(p, ws, strips, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "trellis linear launch");
+  }
+  return TF_OK;
+}
+
+tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr, const void* trellis,
+                           const void* svh, void* y, int out_dtype, int rows, int in_features,
+                           int out_features, int bits, void* stream) {
+  if (rows < 0 || !valid_features(in_features, kMaxInFeatures) ||
+      !valid_features(out_features, kMaxOutFeatures))
+    return TF_ERR_SHAPE;
+  if (!valid_bits(bits)) return TF_ERR_BITS;
+  if (x_dtype != TF_F16 && x_dtype != TF_F32 && x_dtype != TF_BF16) return TF_ERR_DTYPE;
+  if (out_dtype != TF_F16 && out_dtype != TF_F32 && out_dtype != TF_BF16) return TF_ERR_DTYPE;
+  if (rows == 0) return TF_OK;
+  if (!x || !suh || !xr || !trellis || !svh || !y) return TF_ERR_NULL;
+  if (!aligned16(x) || !aligned16(suh) || !aligned16(xr) || !aligned16(trellis) || !aligned16(svh) ||
+      !aligned16(y))
+    return TF_ERR_ALIGN;
+  DeviceCtx* ctx = nullptr;
+  tf_status s = current_ctx(&ctx);
+  if (s != TF_OK) return s;
+  s = check_device_ptrs(ctx->device, x, suh, xr, trellis, svh, y);
+  if (s != TF_OK) return s;
+  s = ensure_workspace(ctx);
+  if (s != TF_OK) return s;
+  TcWorkspace ws;
+  ws.partials = ctx->partials;
+  ws.counters = ctx->counters;
+  ws.err_flag = ctx->err_flag;
+  ws.ctas = trellis_linear_mma_ctas(ctx->num_sms, in_features, out_features, bits);
+  ws.partial_floats_per_cta = kPartialFloatsPerCta;
+  ws.rot_sync = ctx->counters + (ctx->counter_len - 3);
+  const size_t x_elem = x_dtype == TF_F32 ? 4 : 2;
+  const size_t out_elem = out_dtype == TF_F32 ? 4 : 2;
+  const int dt = x_dtype == TF_F16 ? 0 : (x_dtype == TF_F32 ? 1 : 2);
+  for (int r0 = 0; r0 < rows; r0 += kMaxPassRows) {
+    LinearPass p;
+    p.xr = static_cast<const __half*>(xr) + static_cast<size_t>(r0) * in_features;
+    p.trellis = static_cast<const uint32_t*>(trellis);
+    p.svh = static_cast<const __half*>(svh);
+    p.y = static_cast<char*>(y) + static_cast<size_t>(r0) * out_features * out_elem;
+    p.out_dtype = out_dtype;
+    p.rows = rows - r0 < kMaxPassRows ? rows - r0 : kMaxPassRows;
+    p.in_features = in_features;
+    p.out_features = out_features;
+    p.bits = bits;
+    p.rot_x = static_cast<const char*>(x) + static_cast<size_t>(r0) * in_features * x_elem;
+    p.rot_suh = static_cast<const __half*>(suh);
+    p.rot_dtype = dt;
+    cudaError_t e = launch_trellis_linear_mma(p, ws, false, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused rot_in + trellis linear launch");
   }
   return TF_OK;
 }

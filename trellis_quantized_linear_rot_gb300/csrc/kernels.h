@@ -55,6 +55,12 @@ struct LinearPass {
   int in_features;
   int out_features;
   int bits;
+  // The rotation fused into the launch: when rot_x is set, the launch first
+  // writes xr = rot_in(rot_x, rot_suh) for its rows (rot_dtype 0 fp16, 1 fp32,
+  // 2 bf16) into `xr`, then reads it back for the sums.
+  const void* rot_x = nullptr;
+  const __half* rot_suh = nullptr;
+  int rot_dtype = 0;
 };
 
 // Per-device state the linear needs: SM count, error flag, partial-sum
@@ -64,7 +70,8 @@ struct DeviceCtx {
   int num_sms = 0;
   int* err_flag = nullptr;       // device int, OR of error bits
   float* partials = nullptr;     // [slots][16][128] fp32
-  int* counters = nullptr;       // [max_blocks] arrival counters, kept at zero between calls
+  int* counters = nullptr;       // [max_blocks] arrival counters, then the fused rotation's three
+                                 // counts; all kept at zero between calls
   size_t partial_slots = 0;
   size_t counter_len = 0;
 };
@@ -78,6 +85,7 @@ struct TcWorkspace {
   int* err_flag;
   int ctas;
   size_t partial_floats_per_cta;  // capacity per CTA (picks the kernels it can serve)
+  int* rot_sync = nullptr;        // the fused rotation's counts (units handed out, rotated; CTAs done)
 };
 
 int trellis_linear_mma_ctas(int num_sms, int in_features, int out_features, int bits);

@@ -104,6 +104,12 @@ struct MmaParams {
   int rows;
   int in_features;
   int out_features;
+  // The fused rotation (tcgen05 kernel only): null rot_x for none.
+  const void* rot_x = nullptr;
+  const __half* rot_suh = nullptr;
+  __half* rot_xr = nullptr;
+  int* rot_sync = nullptr;
+  int rot_dtype = 0;
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long units, int ctas) {
@@ -553,6 +559,7 @@ cudaError_t launch_one(const CUtensorMap& wmap, const CUtensorMap& xmap, const M
 template <int BITS, int UKT>
 cudaError_t run_mma(const LinearPass& lp, const TcWorkspace& ws, bool strips, cudaStream_t stream) {
   if (strips) return cudaErrorInvalidValue;  // the tcgen05 kernel's order
+  if (lp.rot_x != nullptr) return cudaErrorInvalidValue;  // the fused rotation is the tcgen05 kernel's
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap wmap, xmap;

@@ -75,6 +75,7 @@
 #pragma once
 
 #include "linear_mma.cuh"
+#include "rot_block.cuh"
 
 namespace tfx {
 
@@ -211,6 +212,78 @@ struct RingPos {
   }
 };
 
+// The fused rotation's hand-over between CTAs, on three counts in global
+// memory: sync[0] hands out (row, 128-block) units, sync[1] counts the units
+// rotated, sync[2] the CTAs that are done with both. Units go to whichever
+// warps ask first, so CTAs that start late (their SM still held by the
+// kernel before) leave the rotation to those already running. In each CTA,
+// five actors finish with the counts: the four epilogue warps once a request
+// comes back past the last unit, and the xr producer once it has seen every
+// unit rotated; `fin` (shared memory, zero at the start) counts them, and
+// the CTA's last one counts the CTA into sync[2]. The CTA that completes
+// sync[2] sets all three back to zero: no warp of this launch touches them
+// after that, and the next launch only after this one has ended (its
+// epilogue waits for this kernel first).
+__device__ __forceinline__ void rot_cta_done(int* sync, int ctas, int* fin) {
+  if (atomicAdd(fin, 1) == 4 && atomicAdd(sync + 2, 1) == ctas - 1) {
+    atomicExch(sync, 0);
+    atomicExch(sync + 1, 0);
+    atomicExch(sync + 2, 0);
+  }
+}
+
+// One epilogue warp's part of the rotation: asks for units until they run
+// out, rotates each into xr, then counts the ones it did into sync[1] (after
+// a fence, so that other CTAs that see the count see the rows too).
+template <int DT>
+__device__ __forceinline__ void rot_claim_units(const MmaParams& p, long long units, int lane, int* fin) {
+  const int blocks_per_row = p.in_features >> 7;
+  int done = 0;
+#pragma unroll 1
+  for (;;) {
+    long long u = 0;
+    if (lane == 0) u = atomicAdd(p.rot_sync, 1);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if (u >= units) break;
+    rot_block_warp<DT>(p.rot_x, p.rot_suh, p.rot_xr, static_cast<int>(u / blocks_per_row),
+                       static_cast<int>(u % blocks_per_row), p.in_features, lane);
+    ++done;
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) {
+    if (done > 0) {
+      __threadfence();
+      atomicAdd(p.rot_sync + 1, done);
+    }
+    rot_cta_done(p.rot_sync, p.ctas, fin);
+  }
+}
+
+// The xr producer's wait: lane 0 polls sync[1] (sleeping between tests,
+// bounded by the wait limit of every barrier here) until all `units` are
+// rotated; the warp then orders those writes before its tensor copies.
+// Returns false, with the abort flag set, if the limit passes.
+__device__ __forceinline__ bool rot_wait_all(int* sync, long long units, int ctas, int* fin,
+                                             volatile int* abort_flag, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const unsigned long long t0 = global_ns();
+    while (ld_acquire_gpu(sync + 1) < units) {
+      if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+        ok = 0;
+        *abort_flag = 1;
+        break;
+      }
+      __nanosleep(64);
+    }
+    if (ok) rot_cta_done(sync, ctas, fin);
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  fence_proxy_async_global();  // the rotated rows' generic writes, then this warp's tensor copies of them
+  return ok != 0;
+}
+
 template <int BITS, int LAYOUT, int UKT, int SLOTS>
 __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads, 1)
     trellis_linear_tc_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -232,6 +305,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + T::kMiscOff + 4);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + T::kMiscOff + 8);
+  int* rot_fin = reinterpret_cast<int*>(smem + T::kMiscOff + 12);  // the fused rotation's finished actors
   // Barriers of copy slot us (holding half-unit stages us * CG .. + CG - 1).
   auto wfull_bar = [&](int us) { return bar0 + 8u * us; };
   auto wempty_bar = [&](int us) { return bar0 + 8u * (SUW + us); };
@@ -265,6 +339,7 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     // are multiples of 1024).
     *abort_flag = (smem_u32(smem) & 1023u) != 0 ? 1 : 0;
     *last_flag = 0;
+    *rot_fin = 0;
     for (int us = 0; us < SUW; ++us) {
       mbar_init(wfull_bar(us), 1);
       mbar_init(wempty_bar(us), 4 * CG);  // the 4 warps of each half-unit's decoding warpgroup
@@ -347,7 +422,13 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
     RingPos<SU> rp;
     int h0 = 0;
     int issued = 0;
-    const int n_groups = n_half / CG;
+    // With the rotation fused in, xr is written by this launch's CTAs: no
+    // copy starts before every share is in (none at all if the wait gives up).
+    const bool xr_ready =
+        p.rot_x == nullptr ||
+        rot_wait_all(p.rot_sync, static_cast<long long>(p.rows) * (p.in_features >> 7), p.ctas, rot_fin,
+                     abort_flag, lane);
+    const int n_groups = xr_ready ? n_half / CG : 0;
     for (int u = 0; u < n_groups; ++u) {
       if (u >= SU && !__all_sync(0xffffffffu, mbar_wait(xempty_bar(rp.s), rp.phase ^ 1u, abort_flag))) break;
       const uint32_t st = smem_u32(smem + T::kXRingOff + rp.s * CG * T::kXrBytes);
@@ -534,6 +615,17 @@ __global__ void __launch_bounds__(TcCfg<BITS, SLOTS, UKT / kTcHalfKt>::kThreads,
   } else if (warp < 4) {
     // ----------------------------------------------------------- epilogue
     pdl_wait_prerequisites();  // partial sums, counters and y follow the kernel before
+    if (p.rot_x != nullptr) {
+      // The fused rotation: units of the pass's (row, 128-block) units, as
+      // many as this warp gets, written to xr.
+      const long long nu = static_cast<long long>(p.rows) * (p.in_features >> 7);
+      if (p.rot_dtype == 0)
+        rot_claim_units<0>(p, nu, lane, rot_fin);
+      else if (p.rot_dtype == 1)
+        rot_claim_units<1>(p, nu, lane, rot_fin);
+      else
+        rot_claim_units<2>(p, nu, lane, rot_fin);
+    }
     const int t = threadIdx.x;  // output within the block = Tensor Memory lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     LinearPass lp;
@@ -723,6 +815,14 @@ cudaError_t run_tc_class(const LinearPass& lp, const TcWorkspace& ws, bool strip
   p.rows = lp.rows;
   p.in_features = lp.in_features;
   p.out_features = lp.out_features;
+  if (lp.rot_x != nullptr) {
+    if (ws.rot_sync == nullptr) return cudaErrorInvalidValue;
+    p.rot_x = lp.rot_x;
+    p.rot_suh = lp.rot_suh;
+    p.rot_xr = const_cast<__half*>(lp.xr);
+    p.rot_sync = ws.rot_sync;
+    p.rot_dtype = lp.rot_dtype;
+  }
   return launch_tc<BITS, UKT, SLOTS>(wmap, xmap, p, strips, ws.ctas, stream);
 }
 

@@ -107,6 +107,19 @@ __device__ __forceinline__ bool group_all(int bar_id, int nthreads, bool pred) {
 }
 
 // ------------------------------------------------------------------ fences
+// Orders this thread's generic-proxy accesses to global memory before its
+// later async-proxy ones (tensor copies), and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// A load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
