@@ -350,7 +350,7 @@ def cpu_baseline(all_blocks=60, one_blocks=6):
 
 def fused_calls(args):
     """Whether the step runs the fused call (the k-tile order only)."""
-    return getattr(args, "calls", "fused") == "fused" and args.layout == "tiles"
+    return getattr(args, "calls", "separate") == "fused" and args.layout == "tiles"
 
 
 def bench_config(args, world):
@@ -526,7 +526,7 @@ def run_ours(args):
     ev = {r: [] for r in ROWS}
     call = [0]
 
-    def step(record):
+    def step(record, fused=fused):
         # With `record`, an event pair brackets rot_in and the linear (an
         # event recorded between them would cut the programmatic dependent
         # launch that lets the linear's prologue overlap rot_in; rot_in is
@@ -580,6 +580,22 @@ def run_ours(args):
         for _ in range(args.steps):
             step(True)
         torch.cuda.synchronize()
+        # The same K steps through the other form of the call (the fused
+        # rotation + linear when the headline runs the two calls, and the
+        # other way round), reported beside the headline.
+        alt_ms = None
+        if args.layout == "tiles":
+            for _ in range(args.warmup):
+                step(False, fused=not fused)
+            torch.cuda.synchronize()
+            barrier()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(args.steps):
+                step(False, fused=not fused)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            alt_ms = max_over_ranks(a0.elapsed_time(a1), dist, dev)
     barrier()
     tf.tf_device_error()
     ms_total = max_over_ranks(start.elapsed_time(stop), dist, dev)
@@ -673,6 +689,11 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "f16 (fp32 sums)", "data": "synthetic",
         "config": bench_config(args, world),
         "by_rows": per_rows,
+        "other_calls": None if alt_ms is None else {
+            "calls": ("separate: tf_rot_in then tf_trellis_linear" if fused
+                      else "fused: tf_rot_in_linear, one launch per call"),
+            "ms_per_step": alt_ms / args.steps,
+            "value": replica_value(bytes_step, args.steps, world, alt_ms), "unit": "GB/s"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_avg, "peak_source": peak_kind,
                      "kernel": DOMINANT_KERNEL, "kernel_hash": kernel_hash(),
@@ -712,9 +733,9 @@ def main():
     ap.add_argument("--load-s", type=float, default=0.5,
                     help="untimed steps run under the clock sampler before the timed region (seconds)")
     ap.add_argument("--rows", default="1,8,16", help="row counts per step (default 1,8,16)")
-    ap.add_argument("--calls", choices=["fused", "separate"], default="fused",
-                    help="the step's calls: the fused rotation + linear (default) or rot_in then the linear "
-                         "(always for --layout strips)")
+    ap.add_argument("--calls", choices=["fused", "separate"], default="separate",
+                    help="the headline step's calls: rot_in then the linear (default), or the fused rotation + "
+                         "linear (the k-tile order only); the other form is timed beside it")
     ap.add_argument("--layout", choices=["tiles", "strips"], default="tiles",
                     help="weight storage order: the k-tile-major tiles (the default) or strips "
                          "(repacked once at load, untimed)")
