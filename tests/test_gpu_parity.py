@@ -109,7 +109,7 @@ def test_linear_matches_oracle_small(bits, rows):
 
 
 def test_config_wk_512_to_128_whole_path():
-    """wk 512 -> 128, 4 bits, 1 row, fp16 out: rot_in and linear end to end."""
+    """wk 512 -> 128, 4 bits, 1 row, fp16 out: rot_in and linear end to end (project: the fused call)."""
     i_f, o_f, bits = 512, 128, 4
     x, suh, svh, tr = inputs(1, i_f, o_f, bits, c=0)
     y = host(tf.project(dev(x), dev(suh), dev(tr), dev(svh), bits, o_f, out_dtype=torch.float16))

@@ -248,6 +248,7 @@ def tf_device_error(stream=None):
 
 
 def project(x, suh, trellis, svh, bits, out_features, out_dtype=None, stream=None):
-    """The whole decode-row projection: tf_rot_in then tf_trellis_linear."""
-    xr = tf_rot_in(x, suh, stream=stream)
-    return tf_trellis_linear(xr, trellis, svh, bits, out_features, out_dtype=out_dtype, stream=stream)
+    """The whole decode-row projection (weights in the k-tile-major order), as
+    one fused call: the bits of tf_rot_in then tf_trellis_linear, one launch
+    per pass. Returns y."""
+    return tf_rot_in_linear(x, suh, trellis, svh, bits, out_features, out_dtype=out_dtype, stream=stream)[1]
