@@ -54,7 +54,7 @@ ROWS = (1, 8, 16)
 WORKLOAD = "LM head 5120->129280, 4 bits/weight, rows {1,8,16} per step, fp32 logits"
 METRIC = "weight GB/s and % of HBM peak, trellis linear 5120->129280 @4b, 1-16 rows"
 KERNEL_SOURCES = ("linear_mma.cu", "linear_mma.cuh", "linear_tc.cuh", "decode.cuh", "epilogue.cuh", "ptx.cuh",
-                  "kernels.h")
+                  "kernels.h", "rot_block.cuh")
 DOMINANT_KERNEL = "trellis_linear_tc_kernel"
 L2_BYTES = 129 * 1024 * 1024
 
