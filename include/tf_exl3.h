@@ -138,6 +138,17 @@ tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr
                            void* stream);
 
 /*
+ * tf_rot_in_linear_strips -- tf_rot_in_linear on weights in the strips order
+ * of tf_trellis_linear_strips ("Checks on this head": the strips layout); xr
+ * and y are the bits of tf_rot_in then tf_trellis_linear_strips. Same
+ * arguments, counters and refusals as tf_rot_in_linear.
+ */
+tf_status tf_rot_in_linear_strips(const void* x, int x_dtype, const void* suh, void* xr,
+                                  const void* strips, const void* svh, void* y, int out_dtype,
+                                  int rows, int in_features, int out_features, int bits,
+                                  void* stream);
+
+/*
  * tf_trellis_linear_strips -- tf_trellis_linear on the same tiles stored in
  * the "strips" order ("Checks on this head": the decode test runs on the
  * checkpoint's tile layout and on the strips layout; the page does not spell

@@ -110,8 +110,9 @@ def test_rot_in_refusals(lib):
     assert f(NUL, tf.TF_F16, NUL, NUL, 0, 512, S) == tf.TF_OK
 
 
-def test_rot_in_linear_refusals(lib):
-    f = lib.tf_rot_in_linear
+@pytest.mark.parametrize("name", ["tf_rot_in_linear", "tf_rot_in_linear_strips"])
+def test_rot_in_linear_refusals(lib, name):
+    f = getattr(lib, name)
     def call(x=P, xdt=tf.TF_F16, suh=P, xr=P, tr=P, svh=P, y=P, dt=tf.TF_F32, rows=1, i=512, o=128, bits=4):
         return f(x, xdt, suh, xr, tr, svh, y, dt, rows, i, o, bits, S)
     assert call(rows=-1) == tf.TF_ERR_SHAPE

@@ -87,6 +87,24 @@ def test_fused_is_rot_in_then_linear_bit_for_bit(i_f, o_f, bits, rows, xdt, odt)
     assert np.array_equal(bits_of(y_f), bits_of(y_s))
 
 
+@pytest.mark.parametrize("i_f,o_f,bits,rows", [(5120, 129280, 4, 1), (5120, 129280, 4, 16), (2048, 4096, 6, 24),
+                                                (1024, 2048, 3, 130)])
+def test_fused_strips_is_rot_in_then_strips_linear_bit_for_bit(i_f, o_f, bits, rows):
+    """tf_rot_in_linear_strips: the bits of tf_rot_in then tf_trellis_linear_strips, and of the fused
+    call on the same weights in the k-tile order."""
+    x, suh, svh, tr, x_t, suh_t, svh_t, tr_t = make(rows, i_f, o_f, bits, c=350 + bits)
+    strips_t = tf.tf_trellis_to_strips(tr_t, i_f, o_f, bits)
+    xr_s = tf.tf_rot_in(x_t, suh_t)
+    y_s = tf.tf_trellis_linear_strips(xr_s, strips_t, svh_t, bits, o_f, out_dtype=torch.float32)
+    xr_f, y_f = tf.tf_rot_in_linear(x_t, suh_t, strips_t, svh_t, bits, o_f, out_dtype=torch.float32, strips=True)
+    _, y_t = tf.tf_rot_in_linear(x_t, suh_t, tr_t, svh_t, bits, o_f, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    tf.tf_device_error()
+    assert np.array_equal(bits_of(xr_f), bits_of(xr_s))
+    assert np.array_equal(bits_of(y_f), bits_of(y_s))
+    assert np.array_equal(bits_of(y_f), bits_of(y_t))
+
+
 def test_fused_matches_the_oracle():
     """The fused call against the float64 oracle directly (xr bit-exact with
     the oracle's fp32 rotation, y within the 1e-4 bound), at a shape whose

@@ -25,6 +25,7 @@ SIGNATURES = {
     "tf_rot_in": (_I, [_VP, _I, _VP, _VP, _I, _I, _VP]),
     "tf_trellis_linear": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_rot_in_linear": (_I, [_VP, _I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "tf_rot_in_linear_strips": (_I, [_VP, _I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_linear_strips": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
     "tf_trellis_to_strips": (_I, [_VP, _VP, _I, _I, _I, _VP]),
@@ -153,12 +154,14 @@ def tf_trellis_linear(xr, trellis, svh, bits, out_features, out_dtype=None, y=No
     return y
 
 
-def tf_rot_in_linear(x, suh, trellis, svh, bits, out_features, out_dtype=None, xr=None, y=None, stream=None):
+def tf_rot_in_linear(x, suh, trellis, svh, bits, out_features, out_dtype=None, xr=None, y=None, stream=None,
+                     strips=False):
     """tf_rot_in then tf_trellis_linear in one launch per pass (see tf_rot_in_linear).
 
     x: [rows, in] fp16/bf16/fp32; suh: [in] fp16; trellis in the k-tile-major
-    order; svh: [out] fp16. xr (written, [rows, in] fp16) and y are allocated
-    when not given. Returns (xr, y).
+    order (strips=True: the strips order, tf_rot_in_linear_strips); svh: [out]
+    fp16. xr (written, [rows, in] fp16) and y are allocated when not given.
+    Returns (xr, y).
     """
     import torch
     rows, in_f = x.shape
@@ -170,9 +173,10 @@ def tf_rot_in_linear(x, suh, trellis, svh, bits, out_features, out_dtype=None, x
         y = torch.empty((rows, out_features), dtype=out_dtype or torch.float32, device=x.device)
     _contig(xr, "xr")
     _contig(y, "y")
-    st = lib().tf_rot_in_linear(_ptr(x), _dtype_code(x.dtype), _ptr(suh), _ptr(xr), _ptr(trellis), _ptr(svh),
-                                _ptr(y), _dtype_code(y.dtype), rows, in_f, out_features, bits, _stream(stream))
-    _check(st, "tf_rot_in_linear")
+    f = lib().tf_rot_in_linear_strips if strips else lib().tf_rot_in_linear
+    st = f(_ptr(x), _dtype_code(x.dtype), _ptr(suh), _ptr(xr), _ptr(trellis), _ptr(svh), _ptr(y),
+           _dtype_code(y.dtype), rows, in_f, out_features, bits, _stream(stream))
+    _check(st, "tf_rot_in_linear_strips" if strips else "tf_rot_in_linear")
     return xr, y
 
 

@@ -232,9 +232,9 @@ static tf_status linear_entry(const void* xr, const void* trellis, const void* s
   return TF_OK;
 }
 
-tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr, const void* trellis,
-                           const void* svh, void* y, int out_dtype, int rows, int in_features,
-                           int out_features, int bits, void* stream) {
+static tf_status rot_in_linear_entry(const void* x, int x_dtype, const void* suh, void* xr,
+                                     const void* trellis, const void* svh, void* y, int out_dtype, int rows,
+                                     int in_features, int out_features, int bits, bool strips, void* stream) {
   if (rows < 0 || !valid_features(in_features, kMaxInFeatures) ||
       !valid_features(out_features, kMaxOutFeatures))
     return TF_ERR_SHAPE;
@@ -277,10 +277,24 @@ tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr
     p.rot_x = static_cast<const char*>(x) + static_cast<size_t>(r0) * in_features * x_elem;
     p.rot_suh = static_cast<const __half*>(suh);
     p.rot_dtype = dt;
-    cudaError_t e = launch_trellis_linear_mma(p, ws, false, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_trellis_linear_mma(p, ws, strips, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "fused rot_in + trellis linear launch");
   }
   return TF_OK;
+}
+
+tf_status tf_rot_in_linear(const void* x, int x_dtype, const void* suh, void* xr, const void* trellis,
+                           const void* svh, void* y, int out_dtype, int rows, int in_features,
+                           int out_features, int bits, void* stream) {
+  return rot_in_linear_entry(x, x_dtype, suh, xr, trellis, svh, y, out_dtype, rows, in_features,
+                             out_features, bits, false, stream);
+}
+
+tf_status tf_rot_in_linear_strips(const void* x, int x_dtype, const void* suh, void* xr,
+                                  const void* strips, const void* svh, void* y, int out_dtype, int rows,
+                                  int in_features, int out_features, int bits, void* stream) {
+  return rot_in_linear_entry(x, x_dtype, suh, xr, strips, svh, y, out_dtype, rows, in_features,
+                             out_features, bits, true, stream);
 }
 
 tf_status tf_trellis_linear(const void* xr, const void* trellis, const void* svh, void* y,
