@@ -6,8 +6,7 @@ the linear kernel. Three counters in global memory carry the hand-over:
 count 0 hands units out, count 1 counts the units rotated, and count 2 counts
 the CTAs done with both. In each CTA, five actors take part:
 - the four epilogue warps each ask for units until a request comes back past
-  the last one, rotating each unit they get and adding it to count 1 before
-  the next request;
+  the last one, rotate what they got, and add that to count 1;
 - the xr producer waits until count 1 holds every unit, and only then starts
   its copies of xr.
 A shared-memory count finds the CTA's last actor, which counts the CTA into
@@ -51,6 +50,7 @@ class Launch:
                 self.reset_done = True
 
     def warp(self, c):
+        done = 0
         while True:
             self.touch()
             u = self.sync[0]
@@ -60,9 +60,11 @@ class Launch:
                 break
             assert u not in self.written
             self.written.add(u)       # the rotation's stores (then a fence)
+            done += 1
             yield
+        if done:
             self.touch()
-            self.sync[1] += 1         # counted before the next request
+            self.sync[1] += done
             yield
         self.cta_done(c)
 

@@ -233,13 +233,12 @@ __device__ __forceinline__ void rot_cta_done(int* sync, int ctas, int* fin) {
 }
 
 // One epilogue warp's part of the rotation: asks for units until they run
-// out, rotates each into xr and counts it into sync[1] at once (after a
-// fence, so that other CTAs that see the count see the rows too). Counting
-// each unit before asking for the next keeps the last request's round trip,
-// which comes back past the last unit, out of the time the copies wait.
+// out, rotates each into xr, then counts the ones it did into sync[1] (after
+// a fence, so that other CTAs that see the count see the rows too).
 template <int DT>
 __device__ __forceinline__ void rot_claim_units(const MmaParams& p, long long units, int lane, int* fin) {
   const int blocks_per_row = p.in_features >> 7;
+  int done = 0;
 #pragma unroll 1
   for (;;) {
     long long u = 0;
@@ -248,14 +247,17 @@ __device__ __forceinline__ void rot_claim_units(const MmaParams& p, long long un
     if (u >= units) break;
     rot_block_warp<DT>(p.rot_x, p.rot_suh, p.rot_xr, static_cast<int>(u / blocks_per_row),
                        static_cast<int>(u % blocks_per_row), p.in_features, lane);
-    fence_proxy_async_global();
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(p.rot_sync + 1, 1);
-    }
+    ++done;
   }
-  if (lane == 0) rot_cta_done(p.rot_sync, p.ctas, fin);
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) {
+    if (done > 0) {
+      __threadfence();
+      atomicAdd(p.rot_sync + 1, done);
+    }
+    rot_cta_done(p.rot_sync, p.ctas, fin);
+  }
 }
 
 // The xr producer's wait: lane 0 polls sync[1] (sleeping between tests,
